@@ -1,0 +1,450 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused ZeRO shard-step (params/s and HBM GB/s) on GB300.
+
+One "step" is one optimizer step of the whole workload: for every FSDP unit,
+reduce-scatter by averaging of the N_d bf16 gradient buffers, AdamW on every
+rank's fp32 shard, bf16 cast and all-gather, i.e. one fused zero_step launch
+per unit.  Inputs (gradients, optimizer state) are synthetic and resident in
+HBM before the timed region; they are larger than L2, so no flush is needed.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                  [--workload gpt2-small] [--no-extra]
+
+With N > 1 (launched under torch.distributed.run) every rank runs an
+independent replica of the workload on its own GPU (the path does not shard
+across GPUs); value = all ranks' parameters / max-over-ranks step time.
+`--impl reference` times the CPU oracle on a bounded sample instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "fused ZeRO shard-step params/s and achieved HBM GB/s vs GB300 peak (1 GPU)"
+UNIT = "params/s"
+FALLBACK_HBM_GBS = 6800.0
+WORKLOAD_NAMES = {
+    "gpt2-small": "gpt2-small-124M-13units-Nd8",
+    "llama3-8b-layer": "llama3-8b-decoder-layer-218M-Nd64",
+    "7.5b": "7.5B-32units-Nd64",
+    "tiny": "tiny-4.2M-Nd4",
+}
+
+
+# ------------------------------------------------------------------ env ----
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def init_dist(ws, backend):
+    import torch.distributed as dist
+    if ws > 1 and not dist.is_initialized():
+        os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def barrier(ws):
+    if ws > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, ws: int, device) -> float:
+    if ws <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "fsdp_sharded_mixed_flatten_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str):
+    """DRAM bytes per launch of the fused kernel from a committed ncu summary,
+    or None when the kernel sources changed since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "fused_step_traffic.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+    except Exception:
+        return None
+    if d.get("kernel_source_hash") != kernel_source_hash():
+        return None
+    entry = d.get("workloads", {}).get(workload)
+    return None if entry is None else float(entry["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax = float(parts[1])
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ------------------------------------------------------------- workloads ----
+
+def unit_bytes(P_pad, n_ranks, n_out=1):
+    """Algorithmic HBM bytes of one fused launch: each gradient, state and
+    parameter byte crosses HBM exactly once."""
+    return P_pad * (2 * n_ranks + 24 + 2 * n_out)
+
+
+class Resident:
+    """All units of a workload resident in HBM (per-unit gradient buffers),
+    or, with shared_grads, one gradient buffer reused by every unit (the
+    7.5B model streams its gradients unit by unit)."""
+
+    def __init__(self, w, shared_grads=False, n_units=None):
+        import torch
+        from fsdp_sharded_mixed_flatten_gb300 import synthetic
+        from fsdp_sharded_mixed_flatten_gb300.buffers import FlatUnit
+        self.w = w
+        units = w.units if n_units is None else w.units[:n_units]
+        self.units = []
+        shared = None
+        for ui, u in enumerate(units):
+            fu = FlatUnit(u.numels, w.n_ranks, with_grads=not (shared_grads and shared is not None))
+            if shared_grads:
+                if shared is None:
+                    shared = fu.grads
+                else:
+                    fu.grads = shared
+            master = synthetic.make_master_flat(u.numel, w.n_ranks, w.master_std,
+                                                (w.name, u.name), device="cuda")
+            fu.set_master_flat(master)
+            del master
+            if not (shared_grads and ui > 0):
+                for r in range(w.n_ranks):
+                    synthetic.fill_grad_(fu.grads[r], fu.P, w.grad_std,
+                                         synthetic.seed_for(w.name, u.name, "grad", r),
+                                         w.outlier_frac, w.outlier_scale)
+            self.units.append(fu)
+        torch.cuda.synchronize()
+        self.numel = sum(fu.P for fu in self.units)
+        self.bytes = sum(unit_bytes(fu.P_pad, w.n_ranks) for fu in self.units)
+        self.ptrs = [(fu.grad_rows(), *fu.state_rows(), fu.param_rows(), fu.layout)
+                     for fu in self.units]
+
+    def launch(self, step, hp_base, events=None):
+        from fsdp_sharded_mixed_flatten_gb300 import zero_step
+        hp = dict(hp_base, step=step)
+        for i, (g, ma, m, v, p, lay) in enumerate(self.ptrs):
+            if events is not None:
+                events[i][0].record()
+            zero_step(g, ma, m, v, None, 1, 1, p, lay, hp)
+            if events is not None:
+                events[i][1].record()
+        return len(self.ptrs)
+
+
+def time_resident(res, steps, warmup, ws, device, per_kernel=True, clocks=None):
+    import torch
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    hp = dict(synthetic.ADAMW_DEFAULTS)
+    t = 0
+    for _ in range(warmup):
+        t += 1
+        res.launch(t, hp)
+    torch.cuda.synchronize()
+    n = len(res.units)
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
+           for _ in range(n)] for _ in range(steps)] if per_kernel else None
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.start()
+        time.sleep(0.3)
+    launches = 0
+    start.record()
+    for s in range(steps):
+        t += 1
+        launches += res.launch(t, hp, ev[s] if ev else None)
+    stop.record()
+    torch.cuda.synchronize()
+    clock_info = clocks.stop() if clocks is not None else None
+    barrier(ws)
+    elapsed = start.elapsed_time(stop) / 1e3
+    elapsed_max = max_over_ranks(elapsed, ws, device)
+    kern = None
+    if ev:
+        kern = sum(a.elapsed_time(b) for row in ev for a, b in row) / 1e3
+    return elapsed_max, kern, launches, clock_info
+
+
+def time_e2e(res, steps, warmup, ws, device):
+    """Same step through the public API with host buffers: each step copies
+    every unit's gradients from pinned host memory and reads the gathered
+    bf16 parameters back."""
+    import torch
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    hp = dict(synthetic.ADAMW_DEFAULTS)
+    host_g = [fu.grads.cpu().pin_memory() for fu in res.units]
+    host_p = [torch.empty(fu.params.shape, dtype=torch.bfloat16).pin_memory() for fu in res.units]
+    h2d = sum(x.numel() * 2 for x in host_g)
+    d2h = sum(x.numel() * 2 for x in host_p)
+    from fsdp_sharded_mixed_flatten_gb300 import zero_step
+
+    def one(step):
+        for fu, hg, hpar, ptr in zip(res.units, host_g, host_p, res.ptrs):
+            fu.grads.copy_(hg, non_blocking=True)
+            g, ma, m, v, p, lay = ptr
+            zero_step(g, ma, m, v, None, 1, 1, p, lay, dict(hp, step=step))
+            hpar.copy_(fu.params, non_blocking=True)
+
+    t = 1000
+    for _ in range(warmup):
+        t += 1
+        one(t)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    start.record()
+    for _ in range(steps):
+        t += 1
+        one(t)
+    stop.record()
+    torch.cuda.synchronize()
+    barrier(ws)
+    el = max_over_ranks(start.elapsed_time(stop) / 1e3, ws, device)
+    del host_g, host_p
+    return el, h2d, d2h
+
+
+def cpu_baseline(seconds=8.0):
+    """The CPU oracle as it stands, on a bounded contiguous sample of the
+    gpt2-small workload (first unit, all 8 ranks), single-threaded."""
+    import numpy as np
+    import torch
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    from oracle import Oracle
+    o = Oracle()
+    w = synthetic.workload("gpt2-small")
+    E = 1 << 20
+    g = synthetic.make_grads(E, w.n_ranks, w.grad_std, ("cpu-sample",))
+    gb = synthetic.bf16_bits(g)
+    master = synthetic.make_master_flat(E, w.n_ranks, w.master_std, ("cpu-sample",)).numpy()
+    m = np.zeros_like(master)
+    v = np.zeros_like(master)
+    hp = synthetic.ADAMW_DEFAULTS
+    reps, t0, step = 0, time.perf_counter(), 0
+    while True:
+        step += 1
+        o.sampled_step(gb, master, m, v, step=step, **hp)
+        reps += 1
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            break
+    return {"value": reps * E / el, "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": f"{E} contiguous flat elements x {w.n_ranks} ranks of the gpt2-small "
+                      f"workload, {reps} oracle steps in {el:.1f} s (single thread, double "
+                      f"arithmetic)"}
+
+
+# ----------------------------------------------------------------- arms ----
+
+def run_reference(args, ws, rank):
+    if rank != 0:
+        return 0
+    base = cpu_baseline(seconds=max(2.0, 1.5 * args.steps))
+    line = {"metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "impl": "reference",
+            "config": {"workload": WORKLOAD_NAMES[args.workload], "sample": base["sample"]},
+            "cpu_baseline": base,
+            "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line))
+    return 0
+
+
+def secondary(name, steps, warmup, ws, device, hbm_peak, shared=False, n_units=None):
+    import gc
+    import torch
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    w = synthetic.workload(name)
+    res = Resident(w, shared_grads=shared, n_units=n_units)
+    el, kern, launches, _ = time_resident(res, steps, warmup, ws, device)
+    gbs = res.bytes * steps / kern / 1e9
+    out = {"params_per_s": ws * res.numel * steps / el, "ms_per_step": el / steps * 1e3,
+           "kernel_gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak,
+           "bytes_per_step": res.bytes, "units": len(res.units), "n_ranks": w.n_ranks,
+           "params": res.numel, "steps": steps}
+    del res
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
+def run_ours(args, ws, rank, local):
+    import torch
+    if not torch.cuda.is_available():
+        raise SystemExit("bench.py needs a CUDA device for --impl ours")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    init_dist(ws, "nccl")
+    import fsdp_sharded_mixed_flatten_gb300 as zf
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    zf.load()   # fails loudly if the CUDA library was not built
+    hbm_peak, peak_kind = peaks()
+
+    w = synthetic.workload(args.workload)
+    res = Resident(w)
+    clocks = ClockSampler(local)
+    el, kern, launches, clock_info = time_resident(res, args.steps, args.warmup, ws, device,
+                                                   clocks=clocks)
+    value = ws * res.numel * args.steps / el
+    achieved = res.bytes * args.steps / kern / 1e9
+    traffic = recorded_traffic(args.workload)
+    n_launch = len(res.units)
+    e2e_el, h2d, d2h = time_e2e(res, args.steps, args.warmup, ws, device)
+    e2e = {"value": ws * res.numel * args.steps / e2e_el, "unit": UNIT,
+           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    step_bytes = res.bytes
+    del res
+    import gc
+    gc.collect()
+    torch.cuda.empty_cache()
+
+    extra = {}
+    if not args.no_extra:
+        extra["llama3-8b-decoder-layer-Nd64"] = secondary("llama3-8b-layer", 5, 3, ws, device,
+                                                          hbm_peak)
+        extra["7.5B-32units-Nd64-streamed-grads"] = secondary("7.5b", 2, 1, ws, device,
+                                                              hbm_peak, shared=True)
+
+    base = cpu_baseline() if (rank == 0 and ws == 1) else None
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic",
+        "config": {"workload": WORKLOAD_NAMES[args.workload], "n_ranks_logical": w.n_ranks,
+                   "units": n_launch, "params": sum(u.numel for u in w.units),
+                   "storage": "bf16 grads/params, fp32 master/m/v", "n_out": 1,
+                   "bytes_per_step": step_bytes,
+                   "hbm_gbs_per_step": step_bytes / (el / args.steps) / 1e9,
+                   "l2": "inputs larger than L2 (grads alone 2.0 GB per step)",
+                   "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU, N_d logical ranks"},
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
+                     "frac": achieved / hbm_peak, "peak_kind": peak_kind,
+                     "kernel": "fused_step_kernel",
+                     "traffic": traffic * 1.0 if traffic is not None else None},
+        "cpu_baseline": base,
+        "e2e": e2e,
+        "gpu_launches": launches,
+        "clocks": clock_info,
+        "workloads": extra,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="gpt2-small", choices=list(WORKLOAD_NAMES))
+    ap.add_argument("--no-extra", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        return run_reference(args, ws, rank)
+    return run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

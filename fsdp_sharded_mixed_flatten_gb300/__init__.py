@@ -1,0 +1,19 @@
+"""GB300-native (sm_103a) ZeRO / FSDP sharded mixed-precision step over a
+FlatParameter, with all N_d logical data-parallel ranks held in one GPU.
+
+The compute lives in the CUDA library declared by ``include/zero_flat.h``;
+``zero`` is its thin ctypes binding (same function names), ``buffers`` lays
+out per-rank device buffers with PyTorch allocations, ``synthetic`` draws the
+seeded synthetic workloads, and ``build`` compiles the library in-tree.
+"""
+from .zero import (ZERO_MAX_RANKS, ZeroAdamW, ZeroError, ZeroLayout, load, zero_abi_version,
+                   zero_adamw_shard_step, zero_all_gather, zero_flat_layout, zero_flatten,
+                   zero_last_error, zero_reduce_scatter, zero_shard_segments, zero_step,
+                   zero_unflatten)
+
+__all__ = [
+    "ZERO_MAX_RANKS", "ZeroAdamW", "ZeroError", "ZeroLayout", "load", "zero_abi_version",
+    "zero_adamw_shard_step", "zero_all_gather", "zero_flat_layout", "zero_flatten",
+    "zero_last_error", "zero_reduce_scatter", "zero_shard_segments", "zero_step",
+    "zero_unflatten",
+]

@@ -1,0 +1,438 @@
+// Host side of the C ABI declared in include/zero_flat.h: argument checks,
+// FlatParameter layout, derivation of the fp32 kernel constants in double
+// precision, packing of the per-rank pointer tables into the launch arguments
+// and dispatch to the kernels.  The library allocates nothing and keeps no
+// state apart from a per-thread error message.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <limits>
+
+#include "../../include/zero_flat.h"
+#include "zero_kernels.cuh"
+
+#define ZERO_API extern "C" __attribute__((visibility("default")))
+
+static_assert(zf::kMaxRanks == ZERO_MAX_RANKS, "rank limit mismatch");
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+int fail(int code, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof g_err, fmt, ap);
+    va_end(ap);
+    return code;
+}
+
+int ok() {
+    g_err[0] = '\0';
+    return ZERO_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_layout(const zero_layout_t* L) {
+    if (L == nullptr) return fail(ZERO_ERR_INVALID_ARG, "layout is NULL");
+    if (L->n_ranks < 1) return fail(ZERO_ERR_INVALID_ARG, "n_ranks = %d < 1", L->n_ranks);
+    if (L->n_ranks > ZERO_MAX_RANKS)
+        return fail(ZERO_ERR_SIZE, "n_ranks = %d exceeds %d", L->n_ranks, ZERO_MAX_RANKS);
+    if (L->numel < 1) return fail(ZERO_ERR_INVALID_ARG, "numel = %lld < 1", (long long)L->numel);
+    if (L->n_tensors < 1) return fail(ZERO_ERR_INVALID_ARG, "n_tensors < 1");
+    if (L->shard_numel < 1 || L->numel_padded / L->n_ranks != L->shard_numel ||
+        L->numel_padded % L->n_ranks != 0)
+        return fail(ZERO_ERR_SIZE, "numel_padded != n_ranks * shard_numel");
+    if (L->numel_padded < L->numel || L->numel_padded - L->numel >= L->n_ranks)
+        return fail(ZERO_ERR_SIZE, "numel_padded is not numel rounded up to a multiple of n_ranks");
+    const int64_t tiles = (L->shard_numel + zf::kTile - 1) / zf::kTile;
+    if (tiles * L->n_ranks > std::numeric_limits<int32_t>::max())
+        return fail(ZERO_ERR_SIZE, "flat buffer too large");
+    return ZERO_OK;
+}
+
+template <typename T>
+int check_ptrs(const T* const* ptrs, int n, const char* name, bool allow_null_array = false) {
+    if (ptrs == nullptr) {
+        if (allow_null_array) return ZERO_OK;
+        return fail(ZERO_ERR_INVALID_ARG, "%s is NULL", name);
+    }
+    for (int i = 0; i < n; ++i) {
+        if (ptrs[i] == nullptr) return fail(ZERO_ERR_INVALID_ARG, "%s[%d] is NULL", name, i);
+        if (!aligned16(ptrs[i]))
+            return fail(ZERO_ERR_MISALIGNED, "%s[%d] is not 16-byte aligned", name, i);
+    }
+    return ZERO_OK;
+}
+
+int check_hp(const zero_adamw_t* hp) {
+    if (hp == nullptr) return fail(ZERO_ERR_INVALID_ARG, "hyper-parameters are NULL");
+    const double vals[5] = {hp->lr, hp->beta1, hp->beta2, hp->eps, hp->weight_decay};
+    for (double x : vals)
+        if (!std::isfinite(x)) return fail(ZERO_ERR_INVALID_ARG, "non-finite hyper-parameter");
+    if (hp->lr < 0 || hp->eps < 0 || hp->weight_decay < 0)
+        return fail(ZERO_ERR_INVALID_ARG, "lr, eps and weight_decay must be >= 0");
+    if (hp->beta1 < 0 || hp->beta1 >= 1 || hp->beta2 < 0 || hp->beta2 >= 1)
+        return fail(ZERO_ERR_INVALID_ARG, "betas must lie in [0, 1)");
+    if (hp->step < 1) return fail(ZERO_ERR_INVALID_ARG, "step = %lld < 1", (long long)hp->step);
+    return ZERO_OK;
+}
+
+// fp32 kernel constants from double-precision hyper-parameters: each derived
+// quantity (1 - beta, bias corrections, 1 - lr*wd) is formed in double and
+// rounded once.
+zf::AdamConsts derive_consts(const zero_adamw_t* hp, double divisor) {
+    zf::AdamConsts k{};
+    const double t = static_cast<double>(hp->step);
+    const double bc1 = 1.0 - std::pow(hp->beta1, t);
+    const double bc2 = 1.0 - std::pow(hp->beta2, t);
+    k.beta1 = static_cast<float>(hp->beta1);
+    k.one_minus_beta1 = static_cast<float>(1.0 - hp->beta1);
+    k.beta2 = static_cast<float>(hp->beta2);
+    k.one_minus_beta2 = static_cast<float>(1.0 - hp->beta2);
+    k.eps = static_cast<float>(hp->eps);
+    k.decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
+    k.step_size = static_cast<float>(hp->lr / bc1);
+    k.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
+    k.divisor = static_cast<float>(divisor);
+    return k;
+}
+
+int cuda_status(cudaError_t e, const char* what) {
+    if (e != cudaSuccess)
+        return fail(ZERO_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+    return ok();
+}
+
+int tiles_per_rank(const zero_layout_t* L) {
+    return static_cast<int>((L->shard_numel + zf::kTile - 1) / zf::kTile);
+}
+
+template <int MAXR>
+void fill_step_args(zf::StepArgs<MAXR>& a, const zero_layout_t* L) {
+    a.S = L->shard_numel;
+    a.P_pad = L->numel_padded;
+    a.n_ranks = L->n_ranks;
+    a.n_out = 0;
+    a.tiles_per_rank = tiles_per_rank(L);
+    a.n_ranks_f = static_cast<float>(L->n_ranks);
+    a.inv_n = static_cast<float>(1.0 / static_cast<double>(L->n_ranks));
+    a.n_pow2 = (L->n_ranks & (L->n_ranks - 1)) == 0 ? 1 : 0;
+}
+
+template <int MAXR>
+int run_step(const uint16_t* const* grads, float* const* master, float* const* m,
+             float* const* v, float* const* accum, int32_t micro_step, int32_t n_micro,
+             uint16_t* const* full, int32_t n_out, const zero_layout_t* L,
+             const zero_adamw_t* hp, cudaStream_t stream) {
+    // Up to 24 KB: kept in per-thread static storage rather than on the stack.
+    static thread_local zf::StepArgs<MAXR> args;
+    std::memset(&args, 0, sizeof args);
+    fill_step_args(args, L);
+    const int n = L->n_ranks;
+    for (int k = 0; k < n; ++k) args.grads[k] = grads[k];
+    const bool accumulating = accum != nullptr && n_micro > 1 && micro_step < n_micro;
+    if (accumulating) {
+        for (int r = 0; r < n; ++r) args.accum[r] = accum[r];
+        return cuda_status(zf::launch_reduce_scatter<MAXR>(args, micro_step > 1 ? 1 : 0, stream),
+                           "reduce-scatter launch");
+    }
+    for (int r = 0; r < n; ++r) {
+        args.master[r] = master[r];
+        args.m[r] = m[r];
+        args.v[r] = v[r];
+        if (accum != nullptr && n_micro > 1) args.accum[r] = accum[r];
+    }
+    for (int o = 0; o < n_out; ++o) args.out[o] = full[o];
+    args.n_out = n_out;
+    const bool final_accum = accum != nullptr && n_micro > 1;
+    args.k = derive_consts(hp, final_accum ? static_cast<double>(n_micro) : 1.0);
+    return cuda_status(
+        zf::launch_fused_step<MAXR>(args, final_accum ? zf::kModeAccumFinal : zf::kModePlain, stream),
+        "fused step launch");
+}
+
+}  // namespace
+
+// ------------------------------------------------------------------ API ----
+
+ZERO_API int32_t zero_abi_version(void) { return 1; }
+
+ZERO_API const char* zero_last_error(void) { return g_err; }
+
+ZERO_API int zero_flat_layout(const int64_t* numels, int64_t n_tensors, int32_t n_ranks,
+                              int64_t* offsets_out, zero_layout_t* layout_out) {
+    if (numels == nullptr || offsets_out == nullptr || layout_out == nullptr)
+        return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    if (n_tensors < 1) return fail(ZERO_ERR_INVALID_ARG, "n_tensors < 1");
+    if (n_ranks < 1) return fail(ZERO_ERR_INVALID_ARG, "n_ranks < 1");
+    int64_t total = 0;
+    for (int64_t i = 0; i < n_tensors; ++i) {
+        if (numels[i] < 0) return fail(ZERO_ERR_INVALID_ARG, "numels[%lld] < 0", (long long)i);
+        if (total > std::numeric_limits<int64_t>::max() - numels[i])
+            return fail(ZERO_ERR_SIZE, "total element count overflows int64");
+        offsets_out[i] = total;
+        total += numels[i];
+    }
+    if (total < 1) return fail(ZERO_ERR_INVALID_ARG, "the tensors hold no elements");
+    const int64_t shard = total / n_ranks + (total % n_ranks != 0 ? 1 : 0);
+    if (shard > std::numeric_limits<int64_t>::max() / n_ranks)
+        return fail(ZERO_ERR_SIZE, "padded size overflows int64");
+    layout_out->n_tensors = n_tensors;
+    layout_out->numel = total;
+    layout_out->shard_numel = shard;
+    layout_out->numel_padded = shard * n_ranks;
+    layout_out->n_ranks = n_ranks;
+    layout_out->reserved = 0;
+    return ok();
+}
+
+ZERO_API int zero_shard_segments(const zero_layout_t* L, const int64_t* offsets,
+                                 const int64_t* numels, int32_t rank, int64_t* seg_tensor,
+                                 int64_t* seg_begin, int64_t* seg_end, int64_t cap,
+                                 int64_t* n_seg) {
+    if (int rc = check_layout(L)) return rc;
+    if (offsets == nullptr || numels == nullptr || n_seg == nullptr)
+        return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    if (cap > 0 && (seg_tensor == nullptr || seg_begin == nullptr || seg_end == nullptr))
+        return fail(ZERO_ERR_INVALID_ARG, "NULL output array");
+    if (rank < 0 || rank >= L->n_ranks) return fail(ZERO_ERR_INVALID_ARG, "rank out of range");
+    const int64_t lo = static_cast<int64_t>(rank) * L->shard_numel;
+    const int64_t hi = lo + L->shard_numel;
+    int64_t count = 0;
+    int64_t expect = 0;
+    for (int64_t t = 0; t < L->n_tensors; ++t) {
+        if (offsets[t] != expect || numels[t] < 0)
+            return fail(ZERO_ERR_SIZE, "offsets do not match numels");
+        expect += numels[t];
+        const int64_t b = offsets[t] > lo ? offsets[t] : lo;
+        const int64_t e = offsets[t] + numels[t] < hi ? offsets[t] + numels[t] : hi;
+        if (b < e) {
+            if (count < cap) {
+                seg_tensor[count] = t;
+                seg_begin[count] = b - offsets[t];
+                seg_end[count] = e - offsets[t];
+            }
+            ++count;
+        }
+    }
+    if (expect != L->numel) return fail(ZERO_ERR_SIZE, "numels do not sum to the layout's numel");
+    const int64_t pb = L->numel > lo ? L->numel : lo;
+    if (pb < hi) {
+        if (count < cap) {
+            seg_tensor[count] = -1;
+            seg_begin[count] = pb;
+            seg_end[count] = hi;
+        }
+        ++count;
+    }
+    *n_seg = count;
+    if (count > cap) return fail(ZERO_ERR_SIZE, "cap %lld < %lld pieces", (long long)cap,
+                                 (long long)count);
+    return ok();
+}
+
+static int flatten_impl(const void* const* tensors, const int64_t* offsets, const int64_t* numels,
+                        int32_t elem_bytes, void* const* flat, int32_t split,
+                        const zero_layout_t* L, void* stream, int unflatten) {
+    if (int rc = check_layout(L)) return rc;
+    if (tensors == nullptr || offsets == nullptr || numels == nullptr || flat == nullptr)
+        return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
+    if (elem_bytes != 2 && elem_bytes != 4)
+        return fail(ZERO_ERR_INVALID_ARG, "elem_bytes must be 2 or 4");
+    if (split != 0 && split != 1) return fail(ZERO_ERR_INVALID_ARG, "split must be 0 or 1");
+    const int n_flat = split ? L->n_ranks : 1;
+    if (int rc = check_ptrs(const_cast<const void* const*>(flat), n_flat, "flat buffers")) return rc;
+    int64_t expect = 0;
+    for (int64_t t = 0; t < L->n_tensors; ++t) {
+        if (offsets[t] != expect || numels[t] < 0)
+            return fail(ZERO_ERR_SIZE, "offsets do not match numels");
+        if (numels[t] > 0) {
+            if (tensors[t] == nullptr)
+                return fail(ZERO_ERR_INVALID_ARG, "tensor %lld is NULL", (long long)t);
+            if ((reinterpret_cast<uintptr_t>(tensors[t]) % elem_bytes) != 0)
+                return fail(ZERO_ERR_MISALIGNED, "tensor %lld is not element aligned", (long long)t);
+        }
+        expect += numels[t];
+    }
+    if (expect != L->numel) return fail(ZERO_ERR_SIZE, "numels do not sum to the layout's numel");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    static thread_local zf::FlatArgs a;
+    std::memset(&a, 0, sizeof a);
+    a.S = L->shard_numel;
+    a.split = split;
+    for (int i = 0; i < n_flat; ++i) a.flat[i] = flat[i];
+    for (int64_t t0 = 0; t0 < L->n_tensors; t0 += zf::kFlattenBatch) {
+        const int64_t t1 = t0 + zf::kFlattenBatch < L->n_tensors ? t0 + zf::kFlattenBatch
+                                                                 : L->n_tensors;
+        a.n_tensors = static_cast<int32_t>(t1 - t0);
+        for (int64_t t = t0; t < t1; ++t) {
+            a.tensors[t - t0] = tensors[t];
+            a.off[t - t0] = offsets[t];
+            a.num[t - t0] = numels[t];
+        }
+        a.begin = offsets[t0];
+        a.end = offsets[t1 - 1] + numels[t1 - 1];
+        if (a.end > a.begin) {
+            if (int rc = cuda_status(zf::launch_flatten(a, elem_bytes, unflatten, st), "flatten launch"))
+                return rc;
+        }
+    }
+    if (!unflatten && L->numel_padded > L->numel) {
+        a.n_tensors = 0;
+        a.begin = L->numel;
+        a.end = L->numel_padded;
+        if (int rc = cuda_status(zf::launch_flatten(a, elem_bytes, 0, st), "padding launch")) return rc;
+    }
+    return ok();
+}
+
+ZERO_API int zero_flatten(const void* const* src, const int64_t* offsets, const int64_t* numels,
+                          int32_t elem_bytes, void* const* dst, int32_t dst_split,
+                          const zero_layout_t* L, void* stream) {
+    return flatten_impl(src, offsets, numels, elem_bytes, dst, dst_split, L, stream, 0);
+}
+
+ZERO_API int zero_unflatten(const void* const* src, int32_t src_split, const int64_t* offsets,
+                            const int64_t* numels, int32_t elem_bytes, void* const* dst,
+                            const zero_layout_t* L, void* stream) {
+    // The per-tensor buffers are the destination here; the flat buffer(s) the source.
+    return flatten_impl(const_cast<const void* const*>(dst), offsets, numels, elem_bytes,
+                        const_cast<void* const*>(src), src_split, L, stream, 1);
+}
+
+template <int MAXR>
+static int rs_impl(const uint16_t* const* grads, float* const* grad_shards, const zero_layout_t* L,
+                   int32_t accumulate, cudaStream_t st) {
+    static thread_local zf::StepArgs<MAXR> a;
+    std::memset(&a, 0, sizeof a);
+    fill_step_args(a, L);
+    for (int k = 0; k < L->n_ranks; ++k) {
+        a.grads[k] = grads[k];
+        a.accum[k] = grad_shards[k];
+    }
+    return cuda_status(zf::launch_reduce_scatter<MAXR>(a, accumulate, st), "reduce-scatter launch");
+}
+
+ZERO_API int zero_reduce_scatter(const uint16_t* const* grads, float* const* grad_shards,
+                                 const zero_layout_t* L, int32_t accumulate, void* stream) {
+    if (int rc = check_layout(L)) return rc;
+    const int n = L->n_ranks;
+    if (int rc = check_ptrs(grads, n, "grads")) return rc;
+    if (int rc = check_ptrs(const_cast<const float* const*>(grad_shards), n, "grad_shards"))
+        return rc;
+    if (accumulate != 0 && accumulate != 1)
+        return fail(ZERO_ERR_INVALID_ARG, "accumulate must be 0 or 1");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n <= 64) return rs_impl<64>(grads, grad_shards, L, accumulate, st);
+    return rs_impl<512>(grads, grad_shards, L, accumulate, st);
+}
+
+template <int MAXR>
+static int adamw_impl(float* const* master, float* const* m, float* const* v,
+                      const float* const* grad_shards, float grad_divisor,
+                      uint16_t* const* param_shards, const zero_layout_t* L,
+                      const zero_adamw_t* hp, cudaStream_t st) {
+    static thread_local zf::ShardArgs<MAXR> a;
+    std::memset(&a, 0, sizeof a);
+    a.S = L->shard_numel;
+    a.n_ranks = L->n_ranks;
+    a.tiles_per_rank = tiles_per_rank(L);
+    for (int r = 0; r < L->n_ranks; ++r) {
+        a.master[r] = master[r];
+        a.m[r] = m[r];
+        a.v[r] = v[r];
+        a.grad_shards[r] = grad_shards[r];
+        a.param_shards[r] = param_shards[r];
+    }
+    a.k = derive_consts(hp, static_cast<double>(grad_divisor));
+    return cuda_status(zf::launch_adamw_shards<MAXR>(a, st), "adamw launch");
+}
+
+ZERO_API int zero_adamw_shard_step(float* const* master, float* const* m, float* const* v,
+                                   const float* const* grad_shards, float grad_divisor,
+                                   uint16_t* const* param_shards, const zero_layout_t* L,
+                                   const zero_adamw_t* hp, void* stream) {
+    if (int rc = check_layout(L)) return rc;
+    if (int rc = check_hp(hp)) return rc;
+    const int n = L->n_ranks;
+    if (int rc = check_ptrs(const_cast<const float* const*>(master), n, "master")) return rc;
+    if (int rc = check_ptrs(const_cast<const float* const*>(m), n, "m")) return rc;
+    if (int rc = check_ptrs(const_cast<const float* const*>(v), n, "v")) return rc;
+    if (int rc = check_ptrs(grad_shards, n, "grad_shards")) return rc;
+    if (int rc = check_ptrs(const_cast<const uint16_t* const*>(param_shards), n, "param_shards"))
+        return rc;
+    if (!(grad_divisor > 0.0f) || !std::isfinite(grad_divisor))
+        return fail(ZERO_ERR_INVALID_ARG, "grad_divisor must be a positive finite number");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n <= 64) return adamw_impl<64>(master, m, v, grad_shards, grad_divisor, param_shards, L, hp, st);
+    return adamw_impl<512>(master, m, v, grad_shards, grad_divisor, param_shards, L, hp, st);
+}
+
+template <int MAXR>
+static int gather_impl(const uint16_t* const* param_shards, uint16_t* const* full, int32_t n_out,
+                       const zero_layout_t* L, cudaStream_t st) {
+    static thread_local zf::ShardArgs<MAXR> a;
+    std::memset(&a, 0, sizeof a);
+    a.S = L->shard_numel;
+    a.n_ranks = L->n_ranks;
+    a.n_out = n_out;
+    a.tiles_per_rank = tiles_per_rank(L);
+    for (int r = 0; r < L->n_ranks; ++r) a.param_shards_in[r] = param_shards[r];
+    for (int o = 0; o < n_out; ++o) a.out[o] = full[o];
+    return cuda_status(zf::launch_all_gather<MAXR>(a, st), "all-gather launch");
+}
+
+ZERO_API int zero_all_gather(const uint16_t* const* param_shards, uint16_t* const* full_params,
+                             int32_t n_out, const zero_layout_t* L, void* stream) {
+    if (int rc = check_layout(L)) return rc;
+    if (n_out < 1 || n_out > ZERO_MAX_RANKS)
+        return fail(ZERO_ERR_INVALID_ARG, "n_out must lie in [1, %d]", ZERO_MAX_RANKS);
+    const int n = L->n_ranks;
+    if (int rc = check_ptrs(param_shards, n, "param_shards")) return rc;
+    if (int rc = check_ptrs(const_cast<const uint16_t* const*>(full_params), n_out, "full_params"))
+        return rc;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (n <= 64 && n_out <= 64) return gather_impl<64>(param_shards, full_params, n_out, L, st);
+    return gather_impl<512>(param_shards, full_params, n_out, L, st);
+}
+
+ZERO_API int zero_step(const uint16_t* const* grads, float* const* master, float* const* m,
+                       float* const* v, float* const* accum, int32_t micro_step, int32_t n_micro,
+                       uint16_t* const* full_params, int32_t n_out, const zero_layout_t* L,
+                       const zero_adamw_t* hp, void* stream) {
+    if (int rc = check_layout(L)) return rc;
+    const int n = L->n_ranks;
+    if (int rc = check_ptrs(grads, n, "grads")) return rc;
+    if (accum == nullptr) {
+        if (micro_step != 1 || n_micro != 1)
+            return fail(ZERO_ERR_INVALID_ARG, "micro-stepping needs an accumulator");
+    } else {
+        if (n_micro < 1 || micro_step < 1 || micro_step > n_micro)
+            return fail(ZERO_ERR_INVALID_ARG, "need 1 <= micro_step <= n_micro");
+        if (n_micro > 1) {
+            if (int rc = check_ptrs(const_cast<const float* const*>(accum), n, "accum")) return rc;
+        }
+    }
+    const bool optimizer_runs = accum == nullptr || micro_step == n_micro;
+    if (optimizer_runs) {
+        if (int rc = check_hp(hp)) return rc;
+        if (n_out < 1 || n_out > ZERO_MAX_RANKS)
+            return fail(ZERO_ERR_INVALID_ARG, "n_out must lie in [1, %d]", ZERO_MAX_RANKS);
+        if (int rc = check_ptrs(const_cast<const float* const*>(master), n, "master")) return rc;
+        if (int rc = check_ptrs(const_cast<const float* const*>(m), n, "m")) return rc;
+        if (int rc = check_ptrs(const_cast<const float* const*>(v), n, "v")) return rc;
+        if (int rc = check_ptrs(const_cast<const uint16_t* const*>(full_params), n_out,
+                                "full_params"))
+            return rc;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int need = n > (optimizer_runs ? n_out : 0) ? n : n_out;
+    if (need <= 64)
+        return run_step<64>(grads, master, m, v, accum, micro_step, n_micro, full_params, n_out, L,
+                            hp, st);
+    return run_step<512>(grads, master, m, v, accum, micro_step, n_micro, full_params, n_out, L,
+                         hp, st);
+}

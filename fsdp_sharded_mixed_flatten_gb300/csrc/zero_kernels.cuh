@@ -1,0 +1,86 @@
+// Kernel argument blocks and launcher declarations shared between the host
+// API (zero_api.cu) and the kernel translation units.  Arguments travel by
+// value in the launch (__grid_constant__), so the library needs no device
+// allocation for its pointer tables.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "zero_common.cuh"
+
+namespace zf {
+
+constexpr int kMaxRanks = 512;        // must equal ZERO_MAX_RANKS
+constexpr int kFlattenBatch = 64;     // tensors per flatten / unflatten launch
+
+// Fused step and reduce-scatter.  `accum` doubles as the fp32 gradient-shard
+// output of the reduce-scatter kernel.
+template <int MAXR>
+struct StepArgs {
+    const uint16_t* grads[MAXR];
+    float* master[MAXR];
+    float* m[MAXR];
+    float* v[MAXR];
+    float* accum[MAXR];
+    uint16_t* out[MAXR];
+    int64_t S;
+    int64_t P_pad;
+    int32_t n_ranks;
+    int32_t n_out;
+    int32_t tiles_per_rank;
+    float n_ranks_f;
+    float inv_n;          // 1 / n_ranks (exact when n_ranks is a power of two)
+    int32_t n_pow2;       // n_ranks is a power of two
+    AdamConsts k;
+};
+
+// Unfused AdamW on the shards and all-gather of bf16 shards.
+template <int MAXR>
+struct ShardArgs {
+    const float* grad_shards[MAXR];
+    const uint16_t* param_shards_in[MAXR];
+    float* master[MAXR];
+    float* m[MAXR];
+    float* v[MAXR];
+    uint16_t* param_shards[MAXR];
+    uint16_t* out[MAXR];
+    int64_t S;
+    int32_t n_ranks;
+    int32_t n_out;
+    int32_t tiles_per_rank;
+    AdamConsts k;
+};
+
+// Flatten / unflatten of up to kFlattenBatch tensors covering the flat range
+// [begin, end).  Tensor t occupies [off[t], off[t] + num[t]).
+struct FlatArgs {
+    const void* tensors[kFlattenBatch];
+    int64_t off[kFlattenBatch];
+    int64_t num[kFlattenBatch];
+    void* flat[kMaxRanks];     // one flat buffer, or n_ranks shards
+    int64_t begin;
+    int64_t end;
+    int64_t S;
+    int32_t n_tensors;         // 0: zero-fill (the tail padding)
+    int32_t split;             // flat[] holds n_ranks shards of S elements
+};
+
+enum StepMode : int { kModePlain = 0, kModeAccumFinal = 1 };
+
+// Launchers (return the launch status; grid sizes are chosen inside).
+template <int MAXR>
+cudaError_t launch_fused_step(const StepArgs<MAXR>& a, int mode, cudaStream_t stream);
+template <int MAXR>
+cudaError_t launch_reduce_scatter(const StepArgs<MAXR>& a, int accumulate, cudaStream_t stream);
+template <int MAXR>
+cudaError_t launch_adamw_shards(const ShardArgs<MAXR>& a, cudaStream_t stream);
+template <int MAXR>
+cudaError_t launch_all_gather(const ShardArgs<MAXR>& a, cudaStream_t stream);
+cudaError_t launch_flatten(const FlatArgs& a, int elem_bytes, int unflatten, cudaStream_t stream);
+
+// Persistent grid size: resident CTAs per SM x SMs on the current device,
+// capped by the work available.
+int persistent_grid(const void* kernel, int threads, size_t smem, int64_t work_ctas);
+
+}  // namespace zf

@@ -162,7 +162,7 @@ def fill_grad_(buf: torch.Tensor, numel: int, std: float, seed: int, outlier_fra
         x.mul_(std)
         if outlier_frac > 0.0:
             mask = torch.rand(e - s, generator=g, device=buf.device) < outlier_frac
-            x[mask] *= outlier_scale
+            x = torch.where(mask, x * outlier_scale, x)
         buf[s:e].copy_(x)
     return buf
 

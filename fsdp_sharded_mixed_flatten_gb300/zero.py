@@ -1,0 +1,222 @@
+"""Thin Python binding of the C ABI in include/zero_flat.h (ctypes).
+
+Argument marshalling only: tensors (or raw integer device addresses) are
+turned into pointers, lists into pointer tables, and the current torch CUDA
+stream is passed by default.  Every step of the computation runs in the CUDA
+library; if the library has not been built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+import threading
+from typing import Iterable, List, Sequence, Tuple
+
+from .build import LIB_PATH
+
+ZERO_MAX_RANKS = 512
+ZERO_OK = 0
+ERRORS = {-1: "ZERO_ERR_INVALID_ARG", -2: "ZERO_ERR_MISALIGNED", -3: "ZERO_ERR_SIZE",
+          -4: "ZERO_ERR_CUDA"}
+
+
+class ZeroError(RuntimeError):
+    """A non-OK status from the library (nothing was launched)."""
+
+    def __init__(self, code: int, message: str, func: str):
+        self.code = code
+        self.name = ERRORS.get(code, str(code))
+        super().__init__(f"{func}: {self.name}: {message}")
+
+
+class ZeroLayout(ctypes.Structure):
+    """zero_layout_t: FlatParameter layout of one FSDP unit."""
+    _fields_ = [("n_tensors", ctypes.c_int64), ("numel", ctypes.c_int64),
+                ("numel_padded", ctypes.c_int64), ("shard_numel", ctypes.c_int64),
+                ("n_ranks", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+    def __repr__(self):
+        return (f"ZeroLayout(n_tensors={self.n_tensors}, numel={self.numel}, "
+                f"numel_padded={self.numel_padded}, shard_numel={self.shard_numel}, "
+                f"n_ranks={self.n_ranks})")
+
+
+class ZeroAdamW(ctypes.Structure):
+    """zero_adamw_t: hyper-parameters of one AdamW step (t >= 1)."""
+    _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
+                ("beta2", ctypes.c_double), ("eps", ctypes.c_double),
+                ("weight_decay", ctypes.c_double), ("step", ctypes.c_int64)]
+
+
+_lock = threading.Lock()
+_lib = None
+
+
+def library_path() -> str:
+    return LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load the CUDA library; raise if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is not None:
+            return _lib
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(
+                f"CUDA library {LIB_PATH} is missing: build it with "
+                "`python -m fsdp_sharded_mixed_flatten_gb300.build` (needs nvcc)")
+        lib = ctypes.CDLL(LIB_PATH)
+        p, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        lay, hp = ctypes.POINTER(ZeroLayout), ctypes.POINTER(ZeroAdamW)
+        sig = {
+            "zero_flat_layout": [p, i64, i32, p, lay],
+            "zero_shard_segments": [lay, p, p, i32, p, p, p, i64, p],
+            "zero_flatten": [p, p, p, i32, p, i32, lay, p],
+            "zero_unflatten": [p, i32, p, p, i32, p, lay, p],
+            "zero_reduce_scatter": [p, p, lay, i32, p],
+            "zero_adamw_shard_step": [p, p, p, p, f32, p, lay, hp, p],
+            "zero_all_gather": [p, p, i32, lay, p],
+            "zero_step": [p, p, p, p, p, i32, i32, p, i32, lay, hp, p],
+        }
+        for name, args in sig.items():
+            fn = getattr(lib, name)
+            fn.argtypes = args
+            fn.restype = ctypes.c_int
+        lib.zero_last_error.argtypes = []
+        lib.zero_last_error.restype = ctypes.c_char_p
+        lib.zero_abi_version.argtypes = []
+        lib.zero_abi_version.restype = ctypes.c_int32
+        _lib = lib
+        return lib
+
+
+def header_functions(header: str | None = None) -> List[str]:
+    """Names of the functions include/zero_flat.h declares."""
+    if header is None:
+        header = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))),
+                              "include", "zero_flat.h")
+    text = re.sub(r"/\*.*?\*/", "", open(header).read(), flags=re.S)
+    return sorted(set(re.findall(r"\b(zero_[a-z0-9_]+)\s*\(", text)))
+
+
+# ------------------------------------------------------------ marshalling --
+
+def _addr(x) -> int:
+    if x is None:
+        return 0
+    if isinstance(x, int):
+        return x
+    return int(x.data_ptr())
+
+
+def _ptrs(xs: Sequence):
+    arr = (ctypes.c_void_p * max(len(xs), 1))()
+    for i, x in enumerate(xs):
+        arr[i] = _addr(x) or None
+    return arr
+
+
+def _i64(xs: Iterable[int]):
+    xs = [int(x) for x in xs]
+    return (ctypes.c_int64 * max(len(xs), 1))(*xs)
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        import torch
+        if torch.cuda.is_available():
+            return int(torch.cuda.current_stream().cuda_stream)
+        return 0
+    if isinstance(stream, int):
+        return stream
+    return int(stream.cuda_stream)
+
+
+def _hp(hp) -> ZeroAdamW:
+    if isinstance(hp, ZeroAdamW):
+        return hp
+    if hp is None:
+        return None
+    return ZeroAdamW(float(hp["lr"]), float(hp["beta1"]), float(hp["beta2"]), float(hp["eps"]),
+                     float(hp["weight_decay"]), int(hp["step"]))
+
+
+def _check(rc: int, func: str):
+    if rc != ZERO_OK:
+        raise ZeroError(rc, load().zero_last_error().decode(), func)
+
+
+# ---------------------------------------------------------------- API ------
+
+def zero_abi_version() -> int:
+    return int(load().zero_abi_version())
+
+
+def zero_last_error() -> str:
+    return load().zero_last_error().decode()
+
+
+def zero_flat_layout(numels: Sequence[int], n_ranks: int) -> Tuple[List[int], ZeroLayout]:
+    """Host-only FlatParameter layout: (tensor offsets, layout)."""
+    n = len(numels)
+    offsets = (ctypes.c_int64 * max(n, 1))()
+    layout = ZeroLayout()
+    _check(load().zero_flat_layout(_i64(numels), n, int(n_ranks), offsets, ctypes.byref(layout)),
+           "zero_flat_layout")
+    return [int(offsets[i]) for i in range(n)], layout
+
+
+def zero_shard_segments(layout: ZeroLayout, offsets, numels, rank: int):
+    """Pieces (tensor index or -1 for padding, begin, end) of rank's shard."""
+    lib = load()
+    count = ctypes.c_int64(0)
+    cap = len(numels) + 1
+    t, b, e = (ctypes.c_int64 * cap)(), (ctypes.c_int64 * cap)(), (ctypes.c_int64 * cap)()
+    _check(lib.zero_shard_segments(ctypes.byref(layout), _i64(offsets), _i64(numels), int(rank),
+                                   t, b, e, cap, ctypes.byref(count)), "zero_shard_segments")
+    return [(int(t[i]), int(b[i]), int(e[i])) for i in range(count.value)]
+
+
+def zero_flatten(src, offsets, numels, elem_bytes: int, dst, dst_split: int,
+                 layout: ZeroLayout, stream=None):
+    _check(load().zero_flatten(_ptrs(src), _i64(offsets), _i64(numels), int(elem_bytes),
+                               _ptrs(dst), int(dst_split), ctypes.byref(layout), _stream(stream)),
+           "zero_flatten")
+
+
+def zero_unflatten(src, src_split: int, offsets, numels, elem_bytes: int, dst,
+                   layout: ZeroLayout, stream=None):
+    _check(load().zero_unflatten(_ptrs(src), int(src_split), _i64(offsets), _i64(numels),
+                                 int(elem_bytes), _ptrs(dst), ctypes.byref(layout),
+                                 _stream(stream)), "zero_unflatten")
+
+
+def zero_reduce_scatter(grads, grad_shards, layout: ZeroLayout, accumulate: int = 0, stream=None):
+    _check(load().zero_reduce_scatter(_ptrs(grads), _ptrs(grad_shards), ctypes.byref(layout),
+                                      int(accumulate), _stream(stream)), "zero_reduce_scatter")
+
+
+def zero_adamw_shard_step(master, m, v, grad_shards, grad_divisor: float, param_shards,
+                          layout: ZeroLayout, hp, stream=None):
+    h = _hp(hp)
+    _check(load().zero_adamw_shard_step(_ptrs(master), _ptrs(m), _ptrs(v), _ptrs(grad_shards),
+                                        float(grad_divisor), _ptrs(param_shards),
+                                        ctypes.byref(layout), ctypes.byref(h), _stream(stream)),
+           "zero_adamw_shard_step")
+
+
+def zero_all_gather(param_shards, full_params, layout: ZeroLayout, stream=None):
+    _check(load().zero_all_gather(_ptrs(param_shards), _ptrs(full_params), len(full_params),
+                                  ctypes.byref(layout), _stream(stream)), "zero_all_gather")
+
+
+def zero_step(grads, master, m, v, accum, micro_step: int, n_micro: int, full_params,
+              layout: ZeroLayout, hp, stream=None):
+    h = _hp(hp)
+    _check(load().zero_step(_ptrs(grads), _ptrs(master), _ptrs(m), _ptrs(v),
+                            _ptrs(accum) if accum is not None else None,
+                            int(micro_step), int(n_micro), _ptrs(full_params), len(full_params),
+                            ctypes.byref(layout), ctypes.byref(h) if h is not None else None,
+                            _stream(stream)), "zero_step")

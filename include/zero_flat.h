@@ -1,0 +1,217 @@
+/*
+ * zero_flat.h -- C ABI of the GB300 (sm_103a) ZeRO / FSDP sharded
+ * mixed-precision step over a FlatParameter.
+ *
+ * The method (sources by page title and section):
+ *   [L5] "Lesson 5: ZeRO and FSDP (including the FSDP2 architecture)",
+ *        hpc.payai.win: section 2 (what ZeRO-1/2/3 shard), section 3 (one
+ *        optimizer step = reduce-scatter of the gradients, local update of the
+ *        1/N_d fp32 master/m/v shard and in-place cast to BF16, all-gather of
+ *        the updated shards), section 7.1 (FlatParameter: a unit's tensors are
+ *        flattened into one 1-D buffer, tail-padded to a multiple of the rank
+ *        count, split along the data-parallel dimension).
+ *   [LA] "FSDP", Latent Atlas (process-cxr.github.io): section 5.1 (every rank
+ *        holds an equal contiguous slice of every unit), section 8.2 (bf16
+ *        gradients, fp32 master update).
+ *   [DZ] "Data parallelism and ZeRO memory sharding", jefxiong.cn: section 3.1
+ *        (the synchronised gradient is the mean of the ranks' gradients),
+ *        section 4.2 and the appendix simulator (bias-corrected Adam on each
+ *        rank's slice, then the slices are concatenated).
+ *
+ * All N_d logical data-parallel ranks live in ONE GPU's memory as separate
+ * buffers, so the "collectives" are HBM-streaming kernels, not network calls.
+ *
+ * Conventions shared by every entry point
+ *   - bf16 values travel as uint16_t bit patterns; fp32 as float.
+ *   - Every buffer is owned by the caller.  The library allocates nothing,
+ *     keeps no state between calls and never synchronises the stream.
+ *   - Device-side calls are asynchronous on `stream` (a cudaStream_t, or NULL
+ *     for the legacy default stream) and return after the launch.  The return
+ *     code covers argument checks and launch errors; completion and any later
+ *     kernel fault are observed by synchronising the stream.
+ *   - Pointer arrays (`const T* const* x`) are HOST arrays of DEVICE pointers;
+ *     they are copied into the launch, so they may be freed on return.
+ *   - Every device pointer must be 16-byte aligned (ZERO_ERR_MISALIGNED).
+ *   - Offsets and sizes are element counts (int64_t).
+ *   - Elements [P, P_pad) -- the tail padding -- of the gradients, master, m
+ *     and v must be zero on entry; they then stay zero.
+ *   - Non-finite gradients propagate as NaN/inf through the update.
+ *   - On a non-OK return nothing was launched; zero_last_error() gives a
+ *     message (per calling thread).
+ */
+#ifndef ZERO_FLAT_H
+#define ZERO_FLAT_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Largest supported number of logical ranks N_d and of all-gather outputs. */
+#define ZERO_MAX_RANKS 512
+
+enum {
+    ZERO_OK = 0,
+    ZERO_ERR_INVALID_ARG = -1, /* null pointer, non-positive size, bad hyper-parameter */
+    ZERO_ERR_MISALIGNED = -2,  /* a device pointer is not 16-byte aligned            */
+    ZERO_ERR_SIZE = -3,        /* inconsistent layout, too many ranks, overflow       */
+    ZERO_ERR_CUDA = -4         /* the CUDA runtime reported an error at launch        */
+};
+
+/* FlatParameter layout of one FSDP unit ([L5] section 7.1; [LA] section 5.1). */
+typedef struct zero_layout {
+    int64_t n_tensors;    /* tensors flattened into the unit                   */
+    int64_t numel;        /* P: sum of the tensors' element counts             */
+    int64_t numel_padded; /* P_pad: P rounded up to a multiple of n_ranks      */
+    int64_t shard_numel;  /* S = P_pad / n_ranks; rank r owns [r*S, (r+1)*S)   */
+    int32_t n_ranks;      /* N_d logical data-parallel ranks                   */
+    int32_t reserved;     /* zero                                               */
+} zero_layout_t;
+
+/* AdamW hyper-parameters of one optimizer step ([DZ] section 4.2).  Doubles:
+ * the library derives its fp32 kernel constants (bias corrections included)
+ * in double precision.  Decoupled weight decay theta *= (1 - lr*wd). */
+typedef struct zero_adamw {
+    double lr;            /* >= 0                                   */
+    double beta1;         /* in [0, 1)                              */
+    double beta2;         /* in [0, 1)                              */
+    double eps;           /* >= 0                                   */
+    double weight_decay;  /* >= 0                                   */
+    int64_t step;         /* t >= 1, counts optimizer steps         */
+} zero_adamw_t;
+
+/*
+ * zero_flat_layout -- host only.  ([L5] section 7.1; [LA] section 5.1)
+ * Offsets of the tensors in the flat buffer (prefix sums in the given order,
+ * no gaps and no per-tensor alignment), P, the tail padding to a multiple of
+ * n_ranks, and the shard size S.
+ *   numels[n_tensors]       element count of each tensor (>= 0, sum > 0)
+ *   offsets_out[n_tensors]  receives each tensor's first flat index
+ *   layout_out              receives the layout
+ * Errors: ZERO_ERR_INVALID_ARG (null, n_tensors < 1, n_ranks < 1, a negative
+ * count, total 0), ZERO_ERR_SIZE (the total overflows int64).
+ */
+int zero_flat_layout(const int64_t* numels, int64_t n_tensors, int32_t n_ranks,
+                     int64_t* offsets_out, zero_layout_t* layout_out);
+
+/*
+ * zero_shard_segments -- host only.  ([LA] section 5.1: a rank's slice cuts
+ * across the unit's tensors.)
+ * The pieces of rank `rank`'s shard [r*S, (r+1)*S) in flat order: for piece j,
+ * seg_tensor[j] is the tensor index (or -1 for the tail padding) and
+ * [seg_begin[j], seg_end[j]) the element range inside that tensor (for the
+ * padding: the flat range).  Tensors with zero elements yield no piece.
+ *   cap      capacity of the three output arrays
+ *   n_seg    receives the number of pieces (also when cap is too small)
+ * Errors: ZERO_ERR_INVALID_ARG (null, rank out of range), ZERO_ERR_SIZE
+ * (inconsistent layout, or cap < *n_seg: the arrays hold the first cap pieces).
+ */
+int zero_shard_segments(const zero_layout_t* layout, const int64_t* offsets,
+                        const int64_t* numels, int32_t rank, int64_t* seg_tensor,
+                        int64_t* seg_begin, int64_t* seg_end, int64_t cap, int64_t* n_seg);
+
+/*
+ * zero_flatten -- device.  ([L5] section 7.1: flatten a unit's parameters.)
+ * Copies n_tensors device tensors (elem_bytes = 2 for bf16, 4 for fp32) into
+ * the flat layout and zero-fills the tail padding [P, P_pad).
+ *   src[n_tensors]  device pointers; tensor i has numels[i] elements (a null
+ *                   pointer is allowed only for a tensor with 0 elements)
+ *   offsets, numels HOST arrays as returned / given to zero_flat_layout
+ *   dst             dst_split == 0: dst[0] is one flat buffer of P_pad elements;
+ *                   dst_split == 1: dst[r] (r < n_ranks) is rank r's shard of
+ *                   S elements (e.g. fp32 master weights per rank)
+ * Errors: INVALID_ARG, MISALIGNED (dst only; sources may have any alignment
+ * of their element type), SIZE, CUDA.
+ */
+int zero_flatten(const void* const* src, const int64_t* offsets, const int64_t* numels,
+                 int32_t elem_bytes, void* const* dst, int32_t dst_split,
+                 const zero_layout_t* layout, void* stream);
+
+/*
+ * zero_unflatten -- device.  The inverse view of zero_flatten: copies each
+ * tensor's range of the flat buffer (or of the shards) back into dst[i].
+ * Same arguments with src/dst roles exchanged; padding is not copied.
+ */
+int zero_unflatten(const void* const* src, int32_t src_split, const int64_t* offsets,
+                   const int64_t* numels, int32_t elem_bytes, void* const* dst,
+                   const zero_layout_t* layout, void* stream);
+
+/*
+ * zero_reduce_scatter -- device.  ([L5] section 3, step 1; [DZ] section 3.1.)
+ * Reduce-scatter by averaging: for every rank r and i < S,
+ *   mean = (1/N_d) * sum_{k=0}^{N_d-1} grads[k][r*S + i]
+ * summed in rank order 0..N_d-1 with a compensated fp32 sum (error-free
+ * two-sum), then
+ *   accumulate == 0:  grad_shards[r][i] = mean
+ *   accumulate == 1:  grad_shards[r][i] = grad_shards[r][i] + mean   (fp32)
+ *   grads[n_ranks]        bf16, each P_pad elements (rank k's full gradient)
+ *   grad_shards[n_ranks]  fp32, each S elements
+ */
+int zero_reduce_scatter(const uint16_t* const* grads, float* const* grad_shards,
+                        const zero_layout_t* layout, int32_t accumulate, void* stream);
+
+/*
+ * zero_adamw_shard_step -- device.  ([L5] section 3, step 2; [DZ] section 4.2.)
+ * Every rank's local AdamW update of its fp32 shard and cast to bf16:
+ *   g = grad_shards[r][i] / grad_divisor          (grad_divisor = K averages K
+ *                                                  accumulated micro-steps; 1 = none)
+ *   m = b1*m + (1-b1)*g;   v = b2*v + (1-b2)*g^2
+ *   theta = theta*(1 - lr*wd) - (lr/(1-b1^t)) * m / (sqrt(v)/sqrt(1-b2^t) + eps)
+ *   param_shards[r][i] = bf16_rne(theta)
+ *   master/m/v[n_ranks]    fp32, each S elements, updated in place
+ *   grad_shards[n_ranks]   fp32, each S elements
+ *   param_shards[n_ranks]  bf16, each S elements (output)
+ */
+int zero_adamw_shard_step(float* const* master, float* const* m, float* const* v,
+                          const float* const* grad_shards, float grad_divisor,
+                          uint16_t* const* param_shards, const zero_layout_t* layout,
+                          const zero_adamw_t* hp, void* stream);
+
+/*
+ * zero_all_gather -- device.  ([L5] section 3, step 3; [DZ] appendix: the
+ * updated slices are concatenated once.)
+ *   full_params[o][r*S + i] = param_shards[r][i]   for every o < n_out
+ *   param_shards[n_ranks]  bf16, each S elements
+ *   full_params[n_out]     bf16, each P_pad elements (1 <= n_out <= ZERO_MAX_RANKS)
+ */
+int zero_all_gather(const uint16_t* const* param_shards, uint16_t* const* full_params,
+                    int32_t n_out, const zero_layout_t* layout, void* stream);
+
+/*
+ * zero_step -- device, fused.  The whole step of [L5] section 3 in one pass
+ * over HBM: reduce-scatter by averaging, AdamW on each rank's shard, bf16 cast
+ * and all-gather; neither the fp32 gradient shard nor the bf16 shard is ever
+ * written to memory.  Bit-identical to zero_reduce_scatter +
+ * zero_adamw_shard_step + zero_all_gather on the same inputs.
+ *
+ * Micro-step accumulation ([L5] sections 2 and 3: ZeRO-2 reduce-scatters every
+ * micro-batch into a sharded fp32 accumulator):
+ *   accum == NULL:  micro_step = n_micro = 1; a plain step.
+ *   accum != NULL:  1 <= micro_step <= n_micro;
+ *     micro_step <  n_micro: accum[r] = (micro_step == 1 ? 0 : accum[r]) + mean;
+ *                            no optimizer update, full_params untouched;
+ *     micro_step == n_micro: g = (accum[r] + mean) / n_micro (accum[r] itself is
+ *                            not rewritten), then the update as above
+ *                            (n_micro == 1: g = mean, accum is not touched).
+ *   grads[n_ranks]                 bf16, each P_pad
+ *   master/m/v/accum[n_ranks]      fp32, each S
+ *   full_params[n_out]             bf16, each P_pad
+ *   hp                             read only when the optimizer runs
+ */
+int zero_step(const uint16_t* const* grads, float* const* master, float* const* m,
+              float* const* v, float* const* accum, int32_t micro_step, int32_t n_micro,
+              uint16_t* const* full_params, int32_t n_out, const zero_layout_t* layout,
+              const zero_adamw_t* hp, void* stream);
+
+/* Message for the last non-OK return on the calling thread ("" if none). */
+const char* zero_last_error(void);
+
+/* ABI version of this header (bumped on any incompatible change). */
+int32_t zero_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ZERO_FLAT_H */

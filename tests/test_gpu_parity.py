@@ -1,0 +1,178 @@
+"""CUDA path against the oracle, element by element, through the C ABI.
+
+Sizes here are ones the oracle finishes in seconds; they span many CTA tiles,
+ragged shard ends, every realignment of the gradient slices (S mod 8), padded
+tails, rank counts on both sides of the 64-pointer argument block, several
+all-gather destinations and micro-step accumulation.
+"""
+import numpy as np
+import pytest
+import torch
+
+import parity
+from gpu_harness import Case, bits, hp_at
+
+import fsdp_sharded_mixed_flatten_gb300 as zf
+from fsdp_sharded_mixed_flatten_gb300 import synthetic
+from fsdp_sharded_mixed_flatten_gb300.buffers import FlatUnit, aligned_rows, rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fsdp_sharded_mixed_flatten_gb300 import build
+    build.build()
+    zf.load()
+
+
+def test_tiny_config_ten_steps(oracle):
+    """3 tensors 4096x1024, 1024, 1000; N_d = 4; 10 AdamW steps."""
+    w = synthetic.workload("tiny")
+    c = Case(w.units[0].numels, w.n_ranks, grad_std=w.grad_std, tag="tiny")
+    assert c.S % 8 == 2       # rank slices start off the 16-byte grid
+    for t in range(1, w.steps + 1):
+        c.step(oracle, t)
+    c.compare()
+
+
+CASES = [
+    # (name, numels, n_ranks, n_out, n_micro, steps)
+    ("one_rank", [12345], 1, 1, 1, 3),
+    ("fewer_elements_than_ranks", [5], 8, 1, 1, 3),
+    ("odd_shard_every_realignment", [1000003], 8, 1, 1, 3),
+    ("padded_end_not_multiple_of_8", [999999], 3, 1, 1, 3),
+    ("many_tensors_some_empty", [0, 7, 4099, 0, 1, 65536, 3], 4, 1, 1, 2),
+    ("ranks_64_small_shards", [64 * 37 + 5], 64, 1, 1, 3),
+    ("ranks_65", [65 * 1000 + 7], 65, 1, 1, 2),
+    ("ranks_512", [512 * 33 + 1], 512, 1, 1, 2),
+    ("gather_to_every_rank", [10007], 4, 4, 1, 2),
+    ("accumulate_4_micro_steps", [100003], 8, 1, 4, 2),
+    ("accumulate_3_micro_steps", [40001], 5, 2, 3, 2),
+]
+
+
+@pytest.mark.parametrize("name,numels,n_ranks,n_out,n_micro,steps", CASES,
+                         ids=[c[0] for c in CASES])
+def test_small_cases(oracle, name, numels, n_ranks, n_out, n_micro, steps):
+    c = Case(numels, n_ranks, n_out=n_out, n_micro=n_micro, tag=name)
+    for t in range(1, steps + 1):
+        c.step(oracle, t)
+    c.compare()
+
+
+def test_late_step_bias_corrections(oracle):
+    c = Case([30011], 4, tag="late", hp_over=dict(weight_decay=0.1))
+    c.step(oracle, 10_000)
+    c.step(oracle, 10_001)
+    c.compare()
+
+
+def test_outliers_and_zero_gradients(oracle):
+    c = Case([200003], 16, tag="outliers", outlier_frac=0.05, grad_std=1e-3)
+    c.step(oracle, 1)
+    c.unit.grads.zero_()
+    # a step with all-zero gradients: the moments decay, theta decays
+    hp = hp_at(2)
+    zf.zero_step(c.unit.grad_rows(), *c.unit.state_rows(), None, 1, 1, c.unit.param_rows(),
+                 c.unit.layout, hp)
+    zeros = np.zeros((c.n_ranks, c.P_pad), dtype=np.uint16)
+    c.o_params = oracle.zero_step(zeros, c.o_master, c.o_m, c.o_v, lr=hp["lr"],
+                                  beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
+                                  weight_decay=hp["weight_decay"], step=2)
+    c.compare()
+
+
+@pytest.mark.parametrize("numels,n_ranks", [([4096 * 1024, 1024, 1000], 4), ([1000003], 8),
+                                            ([64 * 1001 + 3], 64), ([77777], 65)])
+def test_reduce_scatter_mean(oracle, numels, n_ranks):
+    """The averaged gradient shard itself against the exact mean."""
+    u = FlatUnit(numels, n_ranks, accum=True)
+    g = synthetic.make_grads(u.P, n_ranks, 1e-2, ("rs", n_ranks), outlier_frac=0.01)
+    # heavy cancellation in a few columns: rank n-1 cancels rank 0
+    if n_ranks > 1:
+        g[-1, :64] = -g[0, :64]
+    u.grads.copy_(g.cuda())
+    zf.zero_reduce_scatter(u.grad_rows(), u.accum_rows(), u.layout, 0)
+    got = u.accum.cpu().numpy().reshape(-1)
+    gb = bits(g)
+    ref = oracle.reduce_scatter(gb).reshape(-1)
+    absmean = np.abs(g.float().numpy()).mean(axis=0)
+    parity.check_mean(got, ref, absmean)
+    exact = np.count_nonzero(got.view(np.uint32) == ref.view(np.uint32)) / got.size
+    assert exact > 0.999, f"only {exact:.5f} of the means are correctly rounded"
+
+
+@pytest.mark.parametrize("numels,n_ranks,n_micro", [([4096 * 1024, 1024, 1000], 4, 1),
+                                                    ([1000003], 8, 1), ([64 * 999 + 1], 64, 2),
+                                                    ([3001], 65, 3)])
+def test_fused_equals_unfused_bitwise(numels, n_ranks, n_micro):
+    """zero_step is bit-identical to reduce-scatter + AdamW + all-gather."""
+    units = [FlatUnit(numels, n_ranks, n_out=2, accum=True) for _ in range(2)]
+    master0 = synthetic.make_master_flat(units[0].P, n_ranks, 0.02, ("fu",)).cuda()
+    for u in units:
+        u.set_master_flat(master0)
+    pshards = aligned_rows(n_ranks, units[0].S, torch.bfloat16, "cuda", 0)
+    for t in (1, 2):
+        hp = hp_at(t)
+        for k in range(1, n_micro + 1):
+            g = synthetic.make_grads(units[0].P, n_ranks, 1e-2, ("fu", t, k)).cuda()
+            for u in units:
+                u.grads.copy_(g)
+            a = units[0]
+            zf.zero_step(a.grad_rows(), *a.state_rows(), a.accum_rows() if n_micro > 1 else None,
+                         k, n_micro, a.param_rows(), a.layout, hp)
+            b = units[1]
+            zf.zero_reduce_scatter(b.grad_rows(), b.accum_rows(), b.layout, 1 if k > 1 else 0)
+            if k == n_micro:
+                zf.zero_adamw_shard_step(*b.state_rows(), b.accum_rows(), float(n_micro),
+                                         rows(pshards), b.layout, hp)
+                zf.zero_all_gather(rows(pshards), b.param_rows(), b.layout)
+    torch.cuda.synchronize()
+    a, b = units
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+        assert torch.equal(x.contiguous().view(torch.int32), y.contiguous().view(torch.int32))
+    assert torch.equal(a.params.contiguous().view(torch.int16),
+                       b.params.contiguous().view(torch.int16))
+    assert torch.equal(a.params[0], a.params[1])
+
+
+def test_flatten_unflatten(oracle):
+    shapes = [(33, 7), (0,), (1000,), (5, 5, 5), (1,), (4099,)]
+    numels = [int(np.prod(s)) for s in shapes]
+    n_ranks = 8
+    off, L = zf.zero_flat_layout(numels, n_ranks)
+    o_off, P, P_pad, S = oracle.flat_layout(numels, n_ranks)
+    assert off == list(o_off)
+    gen = torch.Generator().manual_seed(3)
+    tens = [torch.randn(s, generator=gen).to(torch.bfloat16).cuda() for s in shapes]
+    flat = aligned_rows(1, P_pad, torch.bfloat16, "cuda", 7)  # junk in the padding
+    zf.zero_flatten(tens, off, numels, 2, rows(flat), 0, L)
+    ref = torch.zeros(P_pad, dtype=torch.bfloat16)
+    ref[:P] = torch.cat([t.reshape(-1).cpu() for t in tens])
+    torch.cuda.synchronize()
+    assert torch.equal(flat[0].cpu().view(torch.int16), ref.view(torch.int16))
+    # fp32 into per-rank shards (master weights), then back out
+    tens32 = [torch.randn(s, generator=gen).cuda() for s in shapes]
+    shards = aligned_rows(n_ranks, S, torch.float32, "cuda", -1.0)
+    zf.zero_flatten(tens32, off, numels, 4, rows(shards), 1, L)
+    ref32 = torch.zeros(P_pad)
+    ref32[:P] = torch.cat([t.reshape(-1).cpu() for t in tens32])
+    torch.cuda.synchronize()
+    assert torch.equal(shards.cpu().reshape(-1), ref32)
+    back = [torch.full_like(t, 9.0) for t in tens32]
+    zf.zero_unflatten(rows(shards), 1, off, numels, 4, back, L)
+    torch.cuda.synchronize()
+    for x, y in zip(back, tens32):
+        assert torch.equal(x, y)
+
+
+def test_misaligned_pointer_rejected_without_launch():
+    u = FlatUnit([1000], 4)
+    g = u.grad_rows()
+    bad = [int(x.data_ptr()) + 2 for x in g]
+    with pytest.raises(zf.ZeroError) as ei:
+        zf.zero_step(bad, *u.state_rows(), None, 1, 1, u.param_rows(), u.layout, hp_at(1))
+    assert ei.value.code == -2
