@@ -81,19 +81,24 @@ int check_hp(const zero_adamw_t* hp) {
 }
 
 // fp32 kernel constants from double-precision hyper-parameters: each derived
-// quantity (1 - beta, bias corrections, 1 - lr*wd) is formed in double and
-// rounded once.
+// quantity (1 - beta, bias corrections, lr*wd) is formed in double and rounded
+// once; the moment coefficients are split into (hi, lo) fp32 pairs.
+void split_f32(double x, float& hi, float& lo) {
+    hi = static_cast<float>(x);
+    lo = static_cast<float>(x - static_cast<double>(hi));
+}
+
 zf::AdamConsts derive_consts(const zero_adamw_t* hp, double divisor) {
     zf::AdamConsts k{};
     const double t = static_cast<double>(hp->step);
     const double bc1 = 1.0 - std::pow(hp->beta1, t);
     const double bc2 = 1.0 - std::pow(hp->beta2, t);
-    k.beta1 = static_cast<float>(hp->beta1);
-    k.one_minus_beta1 = static_cast<float>(1.0 - hp->beta1);
-    k.beta2 = static_cast<float>(hp->beta2);
-    k.one_minus_beta2 = static_cast<float>(1.0 - hp->beta2);
+    split_f32(hp->beta1, k.beta1, k.beta1_lo);
+    split_f32(1.0 - hp->beta1, k.one_minus_beta1, k.one_minus_beta1_lo);
+    split_f32(hp->beta2, k.beta2, k.beta2_lo);
+    split_f32(1.0 - hp->beta2, k.one_minus_beta2, k.one_minus_beta2_lo);
     k.eps = static_cast<float>(hp->eps);
-    k.decay = static_cast<float>(1.0 - hp->lr * hp->weight_decay);
+    k.lr_wd = static_cast<float>(hp->lr * hp->weight_decay);
     k.step_size = static_cast<float>(hp->lr / bc1);
     k.inv_sqrt_bc2 = static_cast<float>(1.0 / std::sqrt(bc2));
     k.divisor = static_cast<float>(divisor);

@@ -27,11 +27,15 @@ constexpr int kTile = kThreads * kVec;  // shard elements per CTA tile
 
 // Optimizer constants derived on the host in double precision and rounded
 // once to fp32.
+// The moment coefficients are carried as (hi, lo) fp32 pairs, hi + lo being
+// the double-precision value to ~2^-48: with a single fp32 constant
+// (0.9f = 0.89999998) the moment recursions would pick up a bias of ~3e-8
+// relative per step that accumulates coherently over the steps.
 struct AdamConsts {
-    float beta1, one_minus_beta1;
-    float beta2, one_minus_beta2;
+    float beta1, beta1_lo, one_minus_beta1, one_minus_beta1_lo;
+    float beta2, beta2_lo, one_minus_beta2, one_minus_beta2_lo;
     float eps;
-    float decay;         // 1 - lr * weight_decay
+    float lr_wd;         // lr * weight_decay (decoupled decay theta -= lr*wd*theta)
     float step_size;     // lr / (1 - beta1^t)
     float inv_sqrt_bc2;  // 1 / sqrt(1 - beta2^t)
     float divisor;       // micro-steps averaged (1 for a plain step)
@@ -190,14 +194,19 @@ __device__ __forceinline__ void store_bf16x8(uint16_t* base, int64_t e, int mis,
 //
 // One element of the local shard update: decoupled weight decay, the two
 // moments, bias-corrected step, all in fp32 with explicit round-to-nearest
-// intrinsics (no contraction decided by the compiler), IEEE sqrt and divide.
+// intrinsics (no contraction decided by the compiler), IEEE sqrt and divide:
+//   m' = beta1*m + (1-beta1)*g          v' = beta2*v + (1-beta2)*g^2
+//   theta' = theta - lr*wd*theta - (lr/bc1) * m' / (sqrt(v')/sqrt(bc2) + eps)
 __device__ __forceinline__ void adamw_update(const AdamConsts& k, float g, float& theta,
                                              float& m, float& v) {
-    const float m_new = __fmaf_rn(k.beta1, m, __fmul_rn(k.one_minus_beta1, g));
-    const float v_new = __fmaf_rn(k.beta2, v, __fmul_rn(__fmul_rn(k.one_minus_beta2, g), g));
+    const float corr_m = __fmaf_rn(k.beta1_lo, m, __fmul_rn(k.one_minus_beta1_lo, g));
+    const float m_new = __fmaf_rn(k.beta1, m, __fmaf_rn(k.one_minus_beta1, g, corr_m));
+    const float gg = __fmul_rn(g, g);
+    const float corr_v = __fmaf_rn(k.beta2_lo, v, __fmul_rn(k.one_minus_beta2_lo, gg));
+    const float v_new = __fmaf_rn(k.beta2, v, __fmaf_rn(k.one_minus_beta2, gg, corr_v));
     const float denom = __fmaf_rn(__fsqrt_rn(v_new), k.inv_sqrt_bc2, k.eps);
     const float upd = __fdiv_rn(m_new, denom);
-    const float decayed = __fmul_rn(theta, k.decay);
+    const float decayed = __fmaf_rn(-k.lr_wd, theta, theta);
     theta = __fmaf_rn(-k.step_size, upd, decayed);
     m = m_new;
     v = v_new;

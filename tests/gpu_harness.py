@@ -100,7 +100,9 @@ class Case:
         parity.check_state("master", g_master, self.o_master)
         parity.check_state("m", g_m, self.o_m)
         parity.check_state("v", g_v, self.o_v)
+        flat_master = g_master.reshape(-1)
         for o in range(g_params.shape[0]):
             parity.check_bf16(g_params[o], self.o_params)
+            parity.check_bf16_is_rounded_master(g_params[o], flat_master)
         assert np.all(g_params[:, self.P:] == 0), "padding of the parameters is not zero"
         assert np.all(g_master.reshape(-1)[self.P:] == 0) if self.P_pad > self.P else True

@@ -12,7 +12,9 @@ Derivation (restated in the design notes):
   for the master weights and of 1e-7 * max|ref| (per tensor) for m and v,
   whose values (~1e-4 and ~1e-9 here) make a literal 1e-7 floor vacuous.
 * bf16 parameters: within 1 bf16 ulp (the fp32 masters may sit on either side
-  of a rounding boundary).
+  of a rounding boundary), plus the masters' 1e-7 absolute floor where |theta|
+  is so small that 1e-7 spans many bf16 ulps; >= 99.9 % bit-identical; and
+  always exactly the round-to-nearest-even of the GPU's own fp32 masters.
 """
 from __future__ import annotations
 
@@ -54,9 +56,38 @@ def bf16_ordered(bits):
     return np.where(b & 0x8000, -(b & 0x7FFF), b)
 
 
-def check_bf16(got_bits, ref_bits, max_ulp=1, what="params"):
-    d = np.abs(bf16_ordered(got_bits) - bf16_ordered(ref_bits))
-    bad = np.nonzero(d > max_ulp)[0]
-    assert bad.size == 0, f"{what}: {bad.size} bf16 values more than {max_ulp} ulp apart; " + \
-        _fmt(bad[0], int(np.asarray(got_bits)[bad[0]]), int(np.asarray(ref_bits)[bad[0]]))
-    return int(d.max()) if d.size else 0
+def bf16_value(bits):
+    return (np.asarray(bits).astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+def bf16_ulp(bits):
+    """Spacing of bf16 values at each element's magnitude (2^(e-7); subnormals 2^-133)."""
+    b = np.asarray(bits).astype(np.int64)
+    exp = (b >> 7) & 0xFF
+    return np.where(exp == 0, 2.0 ** -133, np.ldexp(1.0, (np.maximum(exp, 1) - 127 - 7).astype(int)))
+
+
+def check_bf16(got_bits, ref_bits, what="params", min_exact=0.999):
+    """bf16 parameters: within one bf16 ulp of the reference, plus the master
+    weights' absolute floor of 1e-7 (near zero the fp32 masters may differ by
+    up to 1e-7, which is many bf16 ulps there); and almost all exactly equal."""
+    got_bits = np.asarray(got_bits)
+    ref_bits = np.asarray(ref_bits)
+    d = np.abs(bf16_value(got_bits) - bf16_value(ref_bits))
+    tol = bf16_ulp(ref_bits) + 1e-7
+    bad = np.nonzero(d > tol)[0]
+    assert bad.size == 0, f"{what}: {bad.size} bf16 values out of tolerance; " + \
+        _fmt(bad[0], int(got_bits[bad[0]]), int(ref_bits[bad[0]]))
+    exact = float(np.mean(got_bits == ref_bits)) if got_bits.size else 1.0
+    assert exact >= min_exact, f"{what}: only {exact:.6f} of bf16 values match exactly"
+    return int(np.max(np.abs(bf16_ordered(got_bits) - bf16_ordered(ref_bits)))) \
+        if got_bits.size else 0
+
+
+def check_bf16_is_rounded_master(param_bits, master):
+    """The gathered parameters are exactly RNE(master) (PyTorch's conversion)."""
+    import torch
+    m = torch.from_numpy(np.ascontiguousarray(master, dtype=np.float32))
+    ref = m.to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    assert np.array_equal(np.asarray(param_bits, dtype=np.uint16), ref), \
+        "gathered bf16 parameters are not the rounded master weights"

@@ -96,6 +96,7 @@ class SampledUnit:
         parity.check_state("m", g_m, self.o_m)
         parity.check_state("v", g_v, self.o_v)
         parity.check_bf16(g_p, self.o_params)
+        parity.check_bf16_is_rounded_master(g_p, g_master)
         pad = self.idx >= u.P
         assert np.all(g_p[pad] == 0) and np.all(g_master[pad] == 0)
 
