@@ -41,6 +41,13 @@ WORKLOAD_NAMES = {
 }
 
 
+def workload_label(name: str) -> str:
+    if name.startswith("sweep:"):
+        _, p, n = name.split(":")
+        return f"flat-{p}-Nd{n}"
+    return WORKLOAD_NAMES[name]
+
+
 # ------------------------------------------------------------------ env ----
 
 def dist_env():
@@ -237,7 +244,6 @@ def time_resident(res, steps, warmup, ws, device, per_kernel=True, clocks=None):
     torch.cuda.synchronize()
     if clocks is not None:
         clocks.start()
-        time.sleep(0.3)
     launches = 0
     start.record()
     for s in range(steps):
@@ -335,7 +341,7 @@ def run_reference(args, ws, rank):
             "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": WORKLOAD_NAMES[args.workload], "sample": base["sample"]},
+            "config": {"workload": workload_label(args.workload), "sample": base["sample"]},
             "cpu_baseline": base,
             "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
@@ -382,9 +388,11 @@ def run_ours(args, ws, rank, local):
     achieved = res.bytes * args.steps / kern / 1e9
     traffic = recorded_traffic(args.workload)
     n_launch = len(res.units)
-    e2e_el, h2d, d2h = time_e2e(res, args.steps, args.warmup, ws, device)
-    e2e = {"value": ws * res.numel * args.steps / e2e_el, "unit": UNIT,
-           "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+    e2e = None
+    if not args.no_e2e:
+        e2e_el, h2d, d2h = time_e2e(res, args.steps, args.warmup, ws, device)
+        e2e = {"value": ws * res.numel * args.steps / e2e_el, "unit": UNIT,
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
     step_bytes = res.bytes
     del res
     import gc
@@ -398,18 +406,20 @@ def run_ours(args, ws, rank, local):
         extra["7.5B-32units-Nd64-streamed-grads"] = secondary("7.5b", 2, 1, ws, device,
                                                               hbm_peak, shared=True)
 
-    base = cpu_baseline() if (rank == 0 and ws == 1) else None
+    base = cpu_baseline() if (rank == 0 and ws == 1 and not args.no_cpu) else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": WORKLOAD_NAMES[args.workload], "n_ranks_logical": w.n_ranks,
+        "config": {"workload": workload_label(args.workload), "n_ranks_logical": w.n_ranks,
                    "units": n_launch, "params": sum(u.numel for u in w.units),
                    "storage": "bf16 grads/params, fp32 master/m/v", "n_out": 1,
                    "bytes_per_step": step_bytes,
                    "hbm_gbs_per_step": step_bytes / (el / args.steps) / 1e9,
-                   "l2": "inputs larger than L2 (grads alone 2.0 GB per step)",
+                   "l2": "inputs larger than L2 (%.2f GB of gradients per step)" % (
+                       w.n_ranks * sum(synthetic.padded(u.numel, w.n_ranks) for u in w.units)
+                       * 2 / 1e9),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU, N_d logical ranks"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_kind": peak_kind,
@@ -432,12 +442,17 @@ def run_ours(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gpt2-small", choices=list(WORKLOAD_NAMES))
-    ap.add_argument("--no-extra", action="store_true")
+    ap.add_argument("--workload", default="gpt2-small",
+                    help="gpt2-small | llama3-8b-layer | 7.5b | tiny | sweep:<P>:<N_d>")
+    ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
     args = ap.parse_args()
+    if args.workload not in WORKLOAD_NAMES and not args.workload.startswith("sweep:"):
+        ap.error(f"unknown workload {args.workload}")
     if args.warmup < 3:
         args.warmup = 3
     ws, rank, local = dist_env()

@@ -6,15 +6,18 @@
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <limits>
 
-#include "../../include/zero_flat.h"
+#include "zero_flat.h"
 #include "zero_kernels.cuh"
 
 #define ZERO_API extern "C" __attribute__((visibility("default")))
 
 static_assert(zf::kMaxRanks == ZERO_MAX_RANKS, "rank limit mismatch");
+static_assert(zf::kDeviceOk == ZERO_DEVICE_OK && zf::kDeviceTimeout == ZERO_DEVICE_TIMEOUT,
+              "device status codes mismatch");
 
 namespace {
 
@@ -111,6 +114,14 @@ int cuda_status(cudaError_t e, const char* what) {
     return ok();
 }
 
+// Which fused / reduce-scatter kernel runs: the bulk-copy staged one
+// (default) or the direct-load one.  ZERO_STEP_KERNEL=direct selects the
+// latter (both compute bit-identical results); read at every call.
+bool use_staged() {
+    const char* v = std::getenv("ZERO_STEP_KERNEL");
+    return !(v != nullptr && std::strcmp(v, "direct") == 0);
+}
+
 int tiles_per_rank(const zero_layout_t* L) {
     return static_cast<int>((L->shard_numel + zf::kTile - 1) / zf::kTile);
 }
@@ -141,7 +152,12 @@ int run_step(const uint16_t* const* grads, float* const* master, float* const* m
     const bool accumulating = accum != nullptr && n_micro > 1 && micro_step < n_micro;
     if (accumulating) {
         for (int r = 0; r < n; ++r) args.accum[r] = accum[r];
-        return cuda_status(zf::launch_reduce_scatter<MAXR>(args, micro_step > 1 ? 1 : 0, stream),
+        const int acc = micro_step > 1 ? 1 : 0;
+        if (use_staged())
+            return cuda_status(zf::launch_staged_step<MAXR>(
+                                   args, acc ? zf::kModeRsAdd : zf::kModeRsStore, stream),
+                               "reduce-scatter launch");
+        return cuda_status(zf::launch_reduce_scatter<MAXR>(args, acc, stream),
                            "reduce-scatter launch");
     }
     for (int r = 0; r < n; ++r) {
@@ -154,9 +170,10 @@ int run_step(const uint16_t* const* grads, float* const* master, float* const* m
     args.n_out = n_out;
     const bool final_accum = accum != nullptr && n_micro > 1;
     args.k = derive_consts(hp, final_accum ? static_cast<double>(n_micro) : 1.0);
-    return cuda_status(
-        zf::launch_fused_step<MAXR>(args, final_accum ? zf::kModeAccumFinal : zf::kModePlain, stream),
-        "fused step launch");
+    const int mode = final_accum ? zf::kModeAccumFinal : zf::kModePlain;
+    if (use_staged())
+        return cuda_status(zf::launch_staged_step<MAXR>(args, mode, stream), "fused step launch");
+    return cuda_status(zf::launch_fused_step<MAXR>(args, mode, stream), "fused step launch");
 }
 
 }  // namespace
@@ -318,6 +335,10 @@ static int rs_impl(const uint16_t* const* grads, float* const* grad_shards, cons
         a.grads[k] = grads[k];
         a.accum[k] = grad_shards[k];
     }
+    if (use_staged())
+        return cuda_status(zf::launch_staged_step<MAXR>(
+                               a, accumulate ? zf::kModeRsAdd : zf::kModeRsStore, st),
+                           "reduce-scatter launch");
     return cuda_status(zf::launch_reduce_scatter<MAXR>(a, accumulate, st), "reduce-scatter launch");
 }
 
@@ -440,4 +461,21 @@ ZERO_API int zero_step(const uint16_t* const* grads, float* const* master, float
                             hp, st);
     return run_step<512>(grads, master, m, v, accum, micro_step, n_micro, full_params, n_out, L,
                          hp, st);
+}
+
+ZERO_API int zero_device_status(void* stream, int32_t* status, int32_t clear) {
+    if (status == nullptr) return fail(ZERO_ERR_INVALID_ARG, "status is NULL");
+    int v = 0;
+    if (int rc = cuda_status(zf::read_device_status(&v, clear != 0, static_cast<cudaStream_t>(stream)),
+                             "device status read"))
+        return rc;
+    *status = v;
+    return ok();
+}
+
+ZERO_API int zero_selftest_wait_timeout(int64_t limit_ns, void* stream) {
+    if (limit_ns < 1 || limit_ns > 1000000000) return fail(ZERO_ERR_INVALID_ARG, "limit_ns out of range");
+    return cuda_status(zf::launch_wait_timeout_selftest(static_cast<uint64_t>(limit_ns),
+                                                        static_cast<cudaStream_t>(stream)),
+                       "self-test launch");
 }

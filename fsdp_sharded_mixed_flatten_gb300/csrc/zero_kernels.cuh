@@ -66,7 +66,11 @@ struct FlatArgs {
     int32_t split;             // flat[] holds n_ranks shards of S elements
 };
 
-enum StepMode : int { kModePlain = 0, kModeAccumFinal = 1 };
+enum StepMode : int { kModePlain = 0, kModeAccumFinal = 1, kModeRsStore = 2, kModeRsAdd = 3 };
+
+// Device-side status codes (g_zf_device_status); must match ZERO_DEVICE_*.
+constexpr int kDeviceOk = 0;
+constexpr int kDeviceTimeout = 1;
 
 // Launchers (return the launch status; grid sizes are chosen inside).
 template <int MAXR>
@@ -78,6 +82,13 @@ cudaError_t launch_adamw_shards(const ShardArgs<MAXR>& a, cudaStream_t stream);
 template <int MAXR>
 cudaError_t launch_all_gather(const ShardArgs<MAXR>& a, cudaStream_t stream);
 cudaError_t launch_flatten(const FlatArgs& a, int elem_bytes, int unflatten, cudaStream_t stream);
+// Bulk-copy staged fused step / reduce-scatter (mode: StepMode).
+template <int MAXR>
+cudaError_t launch_staged_step(const StepArgs<MAXR>& a, int mode, cudaStream_t stream);
+// One CTA waiting on a barrier that nothing completes (tests the bounded wait).
+cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
+// Read (and optionally clear) the device status word; synchronises `stream`.
+cudaError_t read_device_status(int* status, int clear, cudaStream_t stream);
 
 // Persistent grid size: resident CTAs per SM x SMs on the current device,
 // capped by the work available.

@@ -84,6 +84,10 @@ def load() -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        lib.zero_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_int32), i32]
+        lib.zero_device_status.restype = ctypes.c_int
+        lib.zero_selftest_wait_timeout.argtypes = [i64, p]
+        lib.zero_selftest_wait_timeout.restype = ctypes.c_int
         lib.zero_last_error.argtypes = []
         lib.zero_last_error.restype = ctypes.c_char_p
         lib.zero_abi_version.argtypes = []
@@ -220,3 +224,23 @@ def zero_step(grads, master, m, v, accum, micro_step: int, n_micro: int, full_pa
                             int(micro_step), int(n_micro), _ptrs(full_params), len(full_params),
                             ctypes.byref(layout), ctypes.byref(h) if h is not None else None,
                             _stream(stream)), "zero_step")
+
+
+ZERO_DEVICE_OK = 0
+ZERO_DEVICE_TIMEOUT = 1
+
+
+def zero_device_status(stream=None, clear: bool = True) -> int:
+    """Synchronise the stream and return (and by default clear) the device
+    status word: ZERO_DEVICE_OK, or ZERO_DEVICE_TIMEOUT if a kernel's bounded
+    wait ran out."""
+    v = ctypes.c_int32(0)
+    _check(load().zero_device_status(_stream(stream), ctypes.byref(v), int(bool(clear))),
+           "zero_device_status")
+    return int(v.value)
+
+
+def zero_selftest_wait_timeout(limit_ns: int, stream=None):
+    """Launch a kernel whose bounded barrier wait must run out after limit_ns."""
+    _check(load().zero_selftest_wait_timeout(int(limit_ns), _stream(stream)),
+           "zero_selftest_wait_timeout")

@@ -23,8 +23,9 @@
  *
  * Conventions shared by every entry point
  *   - bf16 values travel as uint16_t bit patterns; fp32 as float.
- *   - Every buffer is owned by the caller.  The library allocates nothing,
- *     keeps no state between calls and never synchronises the stream.
+ *   - Every buffer is owned by the caller.  The library allocates nothing
+ *     and keeps no state between calls except one device status word (see
+ *     zero_device_status); only zero_device_status synchronises a stream.
  *   - Device-side calls are asynchronous on `stream` (a cudaStream_t, or NULL
  *     for the legacy default stream) and return after the launch.  The return
  *     code covers argument checks and launch errors; completion and any later
@@ -203,6 +204,30 @@ int zero_step(const uint16_t* const* grads, float* const* master, float* const* 
               float* const* v, float* const* accum, int32_t micro_step, int32_t n_micro,
               uint16_t* const* full_params, int32_t n_out, const zero_layout_t* layout,
               const zero_adamw_t* hp, void* stream);
+
+/*
+ * zero_device_status -- host, synchronous.  Failure detection for the kernels
+ * that wait on shared-memory barriers (the bulk-copy staged fused step and
+ * reduce-scatter): every such wait gives up after about 2 seconds, records
+ * ZERO_DEVICE_TIMEOUT in a device status word, and the kernel returns early
+ * (its outputs are then incomplete).  This call synchronises `stream`, stores
+ * the word in *status (ZERO_DEVICE_OK when nothing went wrong) and, if clear
+ * != 0, resets it.  No counterpart on the pages: it reports a launch that did
+ * not complete, instead of letting a wait hang the GPU.
+ * Errors: ZERO_ERR_INVALID_ARG (status NULL), ZERO_ERR_CUDA.
+ */
+enum { ZERO_DEVICE_OK = 0, ZERO_DEVICE_TIMEOUT = 1 };
+int zero_device_status(void* stream, int32_t* status, int32_t clear);
+
+/*
+ * zero_selftest_wait_timeout -- device.  Launches one CTA that waits on a
+ * shared-memory barrier nothing ever completes, with the same bounded wait the
+ * staged kernels use but a limit of limit_ns nanoseconds (1 .. 1e9).  The wait
+ * runs out, ZERO_DEVICE_TIMEOUT is recorded and the kernel returns; the
+ * context stays usable.  Exists so that failure detection can be tested
+ * without hanging or faulting the GPU.  No counterpart on the pages.
+ */
+int zero_selftest_wait_timeout(int64_t limit_ns, void* stream);
 
 /* Message for the last non-OK return on the calling thread ("" if none). */
 const char* zero_last_error(void);

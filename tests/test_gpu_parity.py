@@ -54,13 +54,75 @@ CASES = [
 ]
 
 
+@pytest.fixture(params=["staged", "direct"])
+def kernel(request, monkeypatch):
+    """Run a test with the bulk-copy staged kernels (default) and again with
+    the direct-load kernels."""
+    if request.param == "direct":
+        monkeypatch.setenv("ZERO_STEP_KERNEL", "direct")
+    else:
+        monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
+    yield request.param
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
 @pytest.mark.parametrize("name,numels,n_ranks,n_out,n_micro,steps", CASES,
                          ids=[c[0] for c in CASES])
-def test_small_cases(oracle, name, numels, n_ranks, n_out, n_micro, steps):
+def test_small_cases(oracle, kernel, name, numels, n_ranks, n_out, n_micro, steps):
     c = Case(numels, n_ranks, n_out=n_out, n_micro=n_micro, tag=name)
     for t in range(1, steps + 1):
         c.step(oracle, t)
     c.compare()
+
+
+@pytest.mark.parametrize("numels,n_ranks,n_micro", [([4096 * 1024, 1024, 1000], 4, 1),
+                                                    ([999999], 3, 1), ([64 * 4099 + 5], 64, 2),
+                                                    ([77777], 65, 3), ([5], 8, 1)])
+def test_staged_equals_direct_bitwise(monkeypatch, numels, n_ranks, n_micro):
+    """The bulk-copy staged kernels and the direct-load kernels give identical bits."""
+    units = {}
+    master0 = synthetic.make_master_flat(sum(numels),
+                                         n_ranks, 0.02, ("sd",)).cuda()
+    for kern in ("staged", "direct"):
+        if kern == "direct":
+            monkeypatch.setenv("ZERO_STEP_KERNEL", "direct")
+        else:
+            monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
+        u = FlatUnit(numels, n_ranks, n_out=2, accum=True)
+        u.set_master_flat(master0)
+        for t in (1, 2):
+            for k in range(1, n_micro + 1):
+                g = synthetic.make_grads(u.P, n_ranks, 1e-2, ("sd", t, k)).cuda()
+                u.grads.copy_(g)
+                zf.zero_step(u.grad_rows(), *u.state_rows(),
+                             u.accum_rows() if n_micro > 1 else None, k, n_micro,
+                             u.param_rows(), u.layout, hp_at(t))
+        # and a plain reduce-scatter of the last gradients
+        rs = aligned_rows(n_ranks, u.S, torch.float32, "cuda", 0)
+        zf.zero_reduce_scatter(u.grad_rows(), rows(rs), u.layout, 0)
+        torch.cuda.synchronize()
+        units[kern] = (u, rs)
+    monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
+    (a, rsa), (b, rsb) = units["staged"], units["direct"]
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v), (rsa, rsb)):
+        assert torch.equal(x.contiguous().view(torch.int32), y.contiguous().view(torch.int32))
+    assert torch.equal(a.params.contiguous().view(torch.int16),
+                       b.params.contiguous().view(torch.int16))
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
+def test_bounded_wait_reports_timeout():
+    """A barrier wait that nothing satisfies runs out, is reported, and the
+    context stays usable for the next step."""
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+    zf.zero_selftest_wait_timeout(20_000_000)          # 20 ms
+    assert zf.zero_device_status(clear=True) == zf.zero.ZERO_DEVICE_TIMEOUT
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+    u = FlatUnit([4099], 4)
+    u.grads.normal_()
+    zf.zero_step(u.grad_rows(), *u.state_rows(), None, 1, 1, u.param_rows(), u.layout, hp_at(1))
+    torch.cuda.synchronize()
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
 
 
 def test_late_step_bias_corrections(oracle):
