@@ -173,6 +173,26 @@ class ClockSampler:
 
 # ------------------------------------------------------------- workloads ----
 
+# Launch packing of zero_step_units (ZERO_UNITS_PER_LAUNCH, ZERO_POINTERS_PER_LAUNCH in
+# include/zero_flat.h): used only to report how many kernels a step launches.
+UNITS_PER_LAUNCH = 32
+POINTERS_PER_LAUNCH = 3712
+
+
+def staged_launches(n_ranks_per_unit, n_out=1):
+    if os.environ.get("ZERO_STEP_KERNEL") == "direct":
+        return len(n_ranks_per_unit)        # the direct-load kernels: one launch per unit
+    launches, units, ptrs = 0, 0, 0
+    for n in n_ranks_per_unit:
+        need = 4 * n + n_out
+        if units == UNITS_PER_LAUNCH or ptrs + need > POINTERS_PER_LAUNCH or units == 0:
+            launches += 1
+            units, ptrs = 0, 0
+        units += 1
+        ptrs += need
+    return launches
+
+
 def unit_bytes(P_pad, n_ranks, n_out=1):
     """Algorithmic HBM bytes of one fused launch: each gradient, state and
     parameter byte crosses HBM exactly once."""
@@ -212,19 +232,21 @@ class Resident:
         torch.cuda.synchronize()
         self.numel = sum(fu.P for fu in self.units)
         self.bytes = sum(unit_bytes(fu.P_pad, w.n_ranks) for fu in self.units)
-        self.ptrs = [(fu.grad_rows(), *fu.state_rows(), fu.param_rows(), fu.layout)
+        self.ptrs = [(fu.grad_rows(), *fu.state_rows(), None, fu.param_rows(), fu.layout)
                      for fu in self.units]
+        self.launches_per_step = staged_launches([fu.n_ranks for fu in self.units], n_out=1)
 
     def launch(self, step, hp_base, events=None):
-        from fsdp_sharded_mixed_flatten_gb300 import zero_step
+        """One optimizer step over every unit: a single zero_step_units call
+        (the library packs the units into as few launches as it can)."""
+        from fsdp_sharded_mixed_flatten_gb300 import zero_step_units
         hp = dict(hp_base, step=step)
-        for i, (g, ma, m, v, p, lay) in enumerate(self.ptrs):
-            if events is not None:
-                events[i][0].record()
-            zero_step(g, ma, m, v, None, 1, 1, p, lay, hp)
-            if events is not None:
-                events[i][1].record()
-        return len(self.ptrs)
+        if events is not None:
+            events[0][0].record()
+        zero_step_units(self.ptrs, 1, 1, hp)
+        if events is not None:
+            events[0][1].record()
+        return self.launches_per_step
 
 
 def time_resident(res, steps, warmup, ws, device, per_kernel=True, clocks=None):
@@ -236,9 +258,8 @@ def time_resident(res, steps, warmup, ws, device, per_kernel=True, clocks=None):
         t += 1
         res.launch(t, hp)
     torch.cuda.synchronize()
-    n = len(res.units)
-    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]
-           for _ in range(n)] for _ in range(steps)] if per_kernel else None
+    ev = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)]]
+          for _ in range(steps)] if per_kernel else None
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.synchronize()
@@ -272,13 +293,13 @@ def time_e2e(res, steps, warmup, ws, device):
     host_p = [torch.empty(fu.params.shape, dtype=torch.bfloat16).pin_memory() for fu in res.units]
     h2d = sum(x.numel() * 2 for x in host_g)
     d2h = sum(x.numel() * 2 for x in host_p)
-    from fsdp_sharded_mixed_flatten_gb300 import zero_step
+    from fsdp_sharded_mixed_flatten_gb300 import zero_step_units
 
     def one(step):
-        for fu, hg, hpar, ptr in zip(res.units, host_g, host_p, res.ptrs):
+        for fu, hg in zip(res.units, host_g):
             fu.grads.copy_(hg, non_blocking=True)
-            g, ma, m, v, p, lay = ptr
-            zero_step(g, ma, m, v, None, 1, 1, p, lay, dict(hp, step=step))
+        zero_step_units(res.ptrs, 1, 1, dict(hp, step=step))
+        for fu, hpar in zip(res.units, host_p):
             hpar.copy_(fu.params, non_blocking=True)
 
     t = 1000
@@ -423,7 +444,8 @@ def run_ours(args, ws, rank, local):
                    "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU, N_d logical ranks"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_kind": peak_kind,
-                     "kernel": "fused_step_kernel",
+                     "kernel": ("fused_step_kernel" if os.environ.get("ZERO_STEP_KERNEL") == "direct"
+                                else "staged_step_kernel"),
                      "traffic": traffic * 1.0 if traffic is not None else None},
         "cpu_baseline": base,
         "e2e": e2e,
@@ -442,7 +464,7 @@ def run_ours(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2-small",

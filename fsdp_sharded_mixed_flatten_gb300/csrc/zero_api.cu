@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <limits>
+#include <vector>
 
 #include "zero_flat.h"
 #include "zero_kernels.cuh"
@@ -16,6 +17,8 @@
 #define ZERO_API extern "C" __attribute__((visibility("default")))
 
 static_assert(zf::kMaxRanks == ZERO_MAX_RANKS, "rank limit mismatch");
+static_assert(zf::kMaxUnits == ZERO_UNITS_PER_LAUNCH && zf::kMaxPtrs == ZERO_POINTERS_PER_LAUNCH,
+              "launch packing limits mismatch");
 static_assert(zf::kDeviceOk == ZERO_DEVICE_OK && zf::kDeviceTimeout == ZERO_DEVICE_TIMEOUT,
               "device status codes mismatch");
 
@@ -138,42 +141,175 @@ void fill_step_args(zf::StepArgs<MAXR>& a, const zero_layout_t* L) {
     a.n_pow2 = (L->n_ranks & (L->n_ranks - 1)) == 0 ? 1 : 0;
 }
 
+// Host view of one unit for the staged (multi-unit) launches.
+struct UnitView {
+    const zero_layout_t* L;
+    const uint16_t* const* grads;
+    float* const* master;
+    float* const* m;
+    float* const* v;
+    float* const* accum;
+    uint16_t* const* out;
+    int32_t n_out;
+};
+
+int pointers_needed(const UnitView& u, int mode) {
+    const int n = u.L->n_ranks;
+    switch (mode) {
+        case zf::kModePlain: return 4 * n + u.n_out;
+        case zf::kModeAccumFinal: return 5 * n + u.n_out;
+        default: return 2 * n;  // reduce-scatter: gradients + gradient-shard outputs
+    }
+}
+
+// Pack units into as few staged launches as the argument block allows
+// (kMaxUnits units, kMaxPtrs pointers) and launch them in order.
+int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::AdamConsts& k,
+                        cudaStream_t stream) {
+    static thread_local zf::MultiArgs a;
+    int np = 0;
+    a.n_units = 0;
+    a.total_tiles = 0;
+    a.k = k;
+    auto flush = [&]() -> int {
+        if (a.n_units == 0) return ZERO_OK;
+        const int rc = cuda_status(zf::launch_staged_step(a, mode, stream), "staged step launch");
+        a.n_units = 0;
+        a.total_tiles = 0;
+        np = 0;
+        return rc;
+    };
+    for (int i = 0; i < n_units; ++i) {
+        const UnitView& u = units[i];
+        const int n = u.L->n_ranks;
+        const int need = pointers_needed(u, mode);
+        const int64_t tpr = (u.L->shard_numel + zf::kStagedTile - 1) / zf::kStagedTile;
+        const int64_t tiles = tpr * n;
+        if (a.n_units == zf::kMaxUnits || np + need > zf::kMaxPtrs ||
+            static_cast<int64_t>(a.total_tiles) + tiles > std::numeric_limits<int32_t>::max()) {
+            if (int rc = flush()) return rc;
+        }
+        zf::UnitDesc& d = a.unit[a.n_units];
+        d.S = u.L->shard_numel;
+        d.P_pad = u.L->numel_padded;
+        d.n_ranks = n;
+        d.n_out = 0;
+        d.tile_begin = a.total_tiles;
+        d.tiles_per_rank = static_cast<int32_t>(tpr);
+        d.n_ranks_f = static_cast<float>(n);
+        d.inv_n = static_cast<float>(1.0 / static_cast<double>(n));
+        d.n_pow2 = (n & (n - 1)) == 0 ? 1 : 0;
+        d.off_grads = np;
+        for (int r = 0; r < n; ++r) a.ptrs[np++] = u.grads[r];
+        d.off_master = d.off_m = d.off_v = d.off_accum = d.off_out = -1;
+        if (mode == zf::kModePlain || mode == zf::kModeAccumFinal) {
+            d.off_master = np;
+            for (int r = 0; r < n; ++r) a.ptrs[np++] = u.master[r];
+            d.off_m = np;
+            for (int r = 0; r < n; ++r) a.ptrs[np++] = u.m[r];
+            d.off_v = np;
+            for (int r = 0; r < n; ++r) a.ptrs[np++] = u.v[r];
+            d.n_out = u.n_out;
+            d.off_out = np;
+            for (int o = 0; o < u.n_out; ++o) a.ptrs[np++] = u.out[o];
+        }
+        if (mode != zf::kModePlain) {
+            d.off_accum = np;
+            for (int r = 0; r < n; ++r) a.ptrs[np++] = u.accum[r];
+        }
+        a.total_tiles += static_cast<int32_t>(tiles);
+        a.n_units += 1;
+    }
+    return flush();
+}
+
+// One unit's step with the direct-load kernels.
 template <int MAXR>
-int run_step(const uint16_t* const* grads, float* const* master, float* const* m,
-             float* const* v, float* const* accum, int32_t micro_step, int32_t n_micro,
-             uint16_t* const* full, int32_t n_out, const zero_layout_t* L,
-             const zero_adamw_t* hp, cudaStream_t stream) {
+int run_step_direct(const UnitView& u, int32_t micro_step, int32_t n_micro,
+                    const zero_adamw_t* hp, cudaStream_t stream) {
     // Up to 24 KB: kept in per-thread static storage rather than on the stack.
     static thread_local zf::StepArgs<MAXR> args;
     std::memset(&args, 0, sizeof args);
-    fill_step_args(args, L);
-    const int n = L->n_ranks;
-    for (int k = 0; k < n; ++k) args.grads[k] = grads[k];
-    const bool accumulating = accum != nullptr && n_micro > 1 && micro_step < n_micro;
-    if (accumulating) {
-        for (int r = 0; r < n; ++r) args.accum[r] = accum[r];
-        const int acc = micro_step > 1 ? 1 : 0;
-        if (use_staged())
-            return cuda_status(zf::launch_staged_step<MAXR>(
-                                   args, acc ? zf::kModeRsAdd : zf::kModeRsStore, stream),
-                               "reduce-scatter launch");
-        return cuda_status(zf::launch_reduce_scatter<MAXR>(args, acc, stream),
+    fill_step_args(args, u.L);
+    const int n = u.L->n_ranks;
+    for (int k = 0; k < n; ++k) args.grads[k] = u.grads[k];
+    const bool micro = u.accum != nullptr && n_micro > 1;
+    if (micro && micro_step < n_micro) {
+        for (int r = 0; r < n; ++r) args.accum[r] = u.accum[r];
+        return cuda_status(zf::launch_reduce_scatter<MAXR>(args, micro_step > 1 ? 1 : 0, stream),
                            "reduce-scatter launch");
     }
     for (int r = 0; r < n; ++r) {
-        args.master[r] = master[r];
-        args.m[r] = m[r];
-        args.v[r] = v[r];
-        if (accum != nullptr && n_micro > 1) args.accum[r] = accum[r];
+        args.master[r] = u.master[r];
+        args.m[r] = u.m[r];
+        args.v[r] = u.v[r];
+        if (micro) args.accum[r] = u.accum[r];
     }
-    for (int o = 0; o < n_out; ++o) args.out[o] = full[o];
-    args.n_out = n_out;
-    const bool final_accum = accum != nullptr && n_micro > 1;
-    args.k = derive_consts(hp, final_accum ? static_cast<double>(n_micro) : 1.0);
-    const int mode = final_accum ? zf::kModeAccumFinal : zf::kModePlain;
-    if (use_staged())
-        return cuda_status(zf::launch_staged_step<MAXR>(args, mode, stream), "fused step launch");
-    return cuda_status(zf::launch_fused_step<MAXR>(args, mode, stream), "fused step launch");
+    for (int o = 0; o < u.n_out; ++o) args.out[o] = u.out[o];
+    args.n_out = u.n_out;
+    args.k = derive_consts(hp, micro ? static_cast<double>(n_micro) : 1.0);
+    return cuda_status(
+        zf::launch_fused_step<MAXR>(args, micro ? zf::kModeAccumFinal : zf::kModePlain, stream),
+        "fused step launch");
+}
+
+// Validate one unit's arguments for zero_step / zero_step_units.
+int check_unit(const UnitView& u, int32_t micro_step, int32_t n_micro, bool optimizer_runs) {
+    if (int rc = check_layout(u.L)) return rc;
+    const int n = u.L->n_ranks;
+    if (int rc = check_ptrs(u.grads, n, "grads")) return rc;
+    if (u.accum == nullptr) {
+        if (micro_step != 1 || n_micro != 1)
+            return fail(ZERO_ERR_INVALID_ARG, "micro-stepping needs an accumulator");
+    } else {
+        if (n_micro < 1 || micro_step < 1 || micro_step > n_micro)
+            return fail(ZERO_ERR_INVALID_ARG, "need 1 <= micro_step <= n_micro");
+        if (n_micro > 1) {
+            if (int rc = check_ptrs(const_cast<const float* const*>(u.accum), n, "accum")) return rc;
+        }
+    }
+    if (optimizer_runs) {
+        if (u.n_out < 1 || u.n_out > ZERO_MAX_RANKS)
+            return fail(ZERO_ERR_INVALID_ARG, "n_out must lie in [1, %d]", ZERO_MAX_RANKS);
+        if (int rc = check_ptrs(const_cast<const float* const*>(u.master), n, "master")) return rc;
+        if (int rc = check_ptrs(const_cast<const float* const*>(u.m), n, "m")) return rc;
+        if (int rc = check_ptrs(const_cast<const float* const*>(u.v), n, "v")) return rc;
+        if (int rc = check_ptrs(const_cast<const uint16_t* const*>(u.out), u.n_out, "full_params"))
+            return rc;
+    }
+    return ZERO_OK;
+}
+
+int run_units(const UnitView* units, int n_units, int32_t micro_step, int32_t n_micro,
+              const zero_adamw_t* hp, cudaStream_t stream) {
+    // Every unit shares micro_step / n_micro; the optimizer runs unless this is
+    // an accumulation-only micro-step.
+    const bool micro = units[0].accum != nullptr && n_micro > 1;
+    const bool optimizer_runs = !(micro && micro_step < n_micro);
+    if (optimizer_runs) {
+        if (int rc = check_hp(hp)) return rc;
+    }
+    for (int i = 0; i < n_units; ++i) {
+        if ((units[i].accum != nullptr) != (units[0].accum != nullptr))
+            return fail(ZERO_ERR_INVALID_ARG, "either every unit has an accumulator or none");
+        if (int rc = check_unit(units[i], micro_step, n_micro, optimizer_runs)) return rc;
+    }
+    if (use_staged()) {
+        int mode = zf::kModePlain;
+        if (micro) mode = micro_step < n_micro ? (micro_step > 1 ? zf::kModeRsAdd : zf::kModeRsStore)
+                                               : zf::kModeAccumFinal;
+        zf::AdamConsts k{};
+        if (optimizer_runs) k = derive_consts(hp, micro ? static_cast<double>(n_micro) : 1.0);
+        return launch_units_staged(units, n_units, mode, k, stream);
+    }
+    for (int i = 0; i < n_units; ++i) {
+        const UnitView& u = units[i];
+        const int need = u.L->n_ranks > (optimizer_runs ? u.n_out : 0) ? u.L->n_ranks : u.n_out;
+        const int rc = need <= 64 ? run_step_direct<64>(u, micro_step, n_micro, hp, stream)
+                                  : run_step_direct<512>(u, micro_step, n_micro, hp, stream);
+        if (rc) return rc;
+    }
+    return ok();
 }
 
 }  // namespace
@@ -335,10 +471,6 @@ static int rs_impl(const uint16_t* const* grads, float* const* grad_shards, cons
         a.grads[k] = grads[k];
         a.accum[k] = grad_shards[k];
     }
-    if (use_staged())
-        return cuda_status(zf::launch_staged_step<MAXR>(
-                               a, accumulate ? zf::kModeRsAdd : zf::kModeRsStore, st),
-                           "reduce-scatter launch");
     return cuda_status(zf::launch_reduce_scatter<MAXR>(a, accumulate, st), "reduce-scatter launch");
 }
 
@@ -352,6 +484,11 @@ ZERO_API int zero_reduce_scatter(const uint16_t* const* grads, float* const* gra
     if (accumulate != 0 && accumulate != 1)
         return fail(ZERO_ERR_INVALID_ARG, "accumulate must be 0 or 1");
     cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (use_staged()) {
+        const UnitView u{L, grads, nullptr, nullptr, nullptr, grad_shards, nullptr, 0};
+        return launch_units_staged(&u, 1, accumulate ? zf::kModeRsAdd : zf::kModeRsStore,
+                                   zf::AdamConsts{}, st);
+    }
     if (n <= 64) return rs_impl<64>(grads, grad_shards, L, accumulate, st);
     return rs_impl<512>(grads, grad_shards, L, accumulate, st);
 }
@@ -429,38 +566,22 @@ ZERO_API int zero_step(const uint16_t* const* grads, float* const* master, float
                        float* const* v, float* const* accum, int32_t micro_step, int32_t n_micro,
                        uint16_t* const* full_params, int32_t n_out, const zero_layout_t* L,
                        const zero_adamw_t* hp, void* stream) {
-    if (int rc = check_layout(L)) return rc;
-    const int n = L->n_ranks;
-    if (int rc = check_ptrs(grads, n, "grads")) return rc;
-    if (accum == nullptr) {
-        if (micro_step != 1 || n_micro != 1)
-            return fail(ZERO_ERR_INVALID_ARG, "micro-stepping needs an accumulator");
-    } else {
-        if (n_micro < 1 || micro_step < 1 || micro_step > n_micro)
-            return fail(ZERO_ERR_INVALID_ARG, "need 1 <= micro_step <= n_micro");
-        if (n_micro > 1) {
-            if (int rc = check_ptrs(const_cast<const float* const*>(accum), n, "accum")) return rc;
-        }
+    const UnitView u{L, grads, master, m, v, accum, full_params, n_out};
+    return run_units(&u, 1, micro_step, n_micro, hp, static_cast<cudaStream_t>(stream));
+}
+
+ZERO_API int zero_step_units(const zero_unit_t* units, int32_t n_units, int32_t micro_step,
+                             int32_t n_micro, const zero_adamw_t* hp, void* stream) {
+    if (units == nullptr || n_units < 1) return fail(ZERO_ERR_INVALID_ARG, "no units");
+    if (n_units > 4096) return fail(ZERO_ERR_SIZE, "at most 4096 units per call");
+    static thread_local std::vector<UnitView> views;
+    views.resize(static_cast<size_t>(n_units));
+    for (int i = 0; i < n_units; ++i) {
+        const zero_unit_t& x = units[i];
+        views[i] = UnitView{x.layout, x.grads, x.master, x.m, x.v, x.accum, x.full_params, x.n_out};
     }
-    const bool optimizer_runs = accum == nullptr || micro_step == n_micro;
-    if (optimizer_runs) {
-        if (int rc = check_hp(hp)) return rc;
-        if (n_out < 1 || n_out > ZERO_MAX_RANKS)
-            return fail(ZERO_ERR_INVALID_ARG, "n_out must lie in [1, %d]", ZERO_MAX_RANKS);
-        if (int rc = check_ptrs(const_cast<const float* const*>(master), n, "master")) return rc;
-        if (int rc = check_ptrs(const_cast<const float* const*>(m), n, "m")) return rc;
-        if (int rc = check_ptrs(const_cast<const float* const*>(v), n, "v")) return rc;
-        if (int rc = check_ptrs(const_cast<const uint16_t* const*>(full_params), n_out,
-                                "full_params"))
-            return rc;
-    }
-    cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const int need = n > (optimizer_runs ? n_out : 0) ? n : n_out;
-    if (need <= 64)
-        return run_step<64>(grads, master, m, v, accum, micro_step, n_micro, full_params, n_out, L,
-                            hp, st);
-    return run_step<512>(grads, master, m, v, accum, micro_step, n_micro, full_params, n_out, L,
-                         hp, st);
+    return run_units(views.data(), n_units, micro_step, n_micro, hp,
+                     static_cast<cudaStream_t>(stream));
 }
 
 ZERO_API int zero_device_status(void* stream, int32_t* status, int32_t clear) {

@@ -66,6 +66,40 @@ struct FlatArgs {
     int32_t split;             // flat[] holds n_ranks shards of S elements
 };
 
+// Bulk-copy staged kernels: argument block covering up to kMaxUnits units
+// (FlatParameters) whose per-rank pointers live in one flat table.
+constexpr int kStagedTile = 4096;   // shard elements per tile (512 consumers x 8)
+constexpr int kMaxUnits = 32;
+constexpr int kMaxPtrs = 3712;
+
+struct UnitDesc {
+    int64_t S;
+    int64_t P_pad;
+    int32_t n_ranks;
+    int32_t n_out;
+    int32_t tile_begin;       // first tile of this unit in the launch's tile sequence
+    int32_t tiles_per_rank;   // ceil(S / kStagedTile)
+    int32_t off_grads;        // ptrs[off_grads + k]: rank k's bf16 gradient buffer
+    int32_t off_master;       // ptrs[off_master + r] (and off_m, off_v): fp32 state shards
+    int32_t off_m;
+    int32_t off_v;
+    int32_t off_accum;        // fp32 accumulator / gradient-shard output
+    int32_t off_out;          // ptrs[off_out + o]: bf16 gathered parameters
+    float n_ranks_f;
+    float inv_n;
+    int32_t n_pow2;
+};
+
+struct MultiArgs {
+    int32_t n_units;
+    int32_t total_tiles;
+    AdamConsts k;
+    UnitDesc unit[kMaxUnits];
+    const void* ptrs[kMaxPtrs];
+};
+
+static_assert(sizeof(MultiArgs) <= 32764, "launch argument block limit");
+
 enum StepMode : int { kModePlain = 0, kModeAccumFinal = 1, kModeRsStore = 2, kModeRsAdd = 3 };
 
 // Device-side status codes (g_zf_device_status); must match ZERO_DEVICE_*.
@@ -82,9 +116,8 @@ cudaError_t launch_adamw_shards(const ShardArgs<MAXR>& a, cudaStream_t stream);
 template <int MAXR>
 cudaError_t launch_all_gather(const ShardArgs<MAXR>& a, cudaStream_t stream);
 cudaError_t launch_flatten(const FlatArgs& a, int elem_bytes, int unflatten, cudaStream_t stream);
-// Bulk-copy staged fused step / reduce-scatter (mode: StepMode).
-template <int MAXR>
-cudaError_t launch_staged_step(const StepArgs<MAXR>& a, int mode, cudaStream_t stream);
+// Bulk-copy staged fused step / reduce-scatter over the units of `a` (mode: StepMode).
+cudaError_t launch_staged_step(const MultiArgs& a, int mode, cudaStream_t stream);
 // One CTA waiting on a barrier that nothing completes (tests the bounded wait).
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 // Read (and optionally clear) the device status word; synchronises `stream`.

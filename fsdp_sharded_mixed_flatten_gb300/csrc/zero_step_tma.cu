@@ -1,16 +1,25 @@
-// Bulk-copy (TMA) staged variant of the fused step and of the reduce-scatter.
+// Bulk-copy (TMA) staged fused step and reduce-scatter, over one or many
+// FlatParameters (FSDP units) per launch.
 //
 // Same arithmetic, element order and results as zero_step.cu (bit-identical);
 // what changes is how the bytes reach the SM.  One producer lane per CTA
-// streams every byte the tile reads -- the tile's fp32 state (master, m, v,
-// accumulator) and, rank group by rank group, the N_d bf16 gradient slices --
+// streams every byte a tile reads -- the tile's fp32 state (master, m, v,
+// accumulator) and, eight ranks per stage, the N_d bf16 gradient slices --
 // into a ring of shared-memory stages with cp.async.bulk (the Blackwell TMA
-// engine, plain global->shared copies, completion counted in bytes on an
-// mbarrier).  Eight consumer warps wait on a stage, read their 8 elements per
-// rank from shared memory, release the stage and finally run AdamW and write
-// the results.  The ring keeps up to kStages * 32 KB in flight per SM
-// independently of the consumers' registers, which the direct-load kernel
-// cannot (its in-flight bytes are bounded by its loads in registers).
+// engine: plain global->shared copies whose completion is counted in bytes on
+// an mbarrier).  Sixteen consumer warps wait on a stage, read their 8 elements
+// per rank from shared memory, release the stage and finally run AdamW and
+// write the results.  A tile is 4096 elements of one rank's shard of one unit,
+// so every gradient copy is an 8 KB contiguous run of one buffer; the ring
+// keeps up to 3 x 64 KB in flight per SM independently of the consumers'
+// registers, which the direct-load kernel cannot (its in-flight bytes are
+// bounded by the loads it holds in registers).  Measured on GB300: with 8
+// consumer warps per SM the kernel stayed issue/latency-bound near 70 % of
+// the HBM bandwidth; 16 consumer warps reach it.
+//
+// One launch may cover several units (the tiles of all units form one global
+// tile sequence), so small units do not each pay a launch, a pipeline fill
+// and a tail.
 //
 // Copies must start on 16-byte boundaries: a rank's slice of a tile starts at
 // flat element r*S + j0, so the copied range is widened down to a multiple of
@@ -19,8 +28,8 @@
 // threads that own it read it from global memory.
 //
 // Every wait is bounded (kWaitLimitNs of wall time on %globaltimer).  A wait
-// that runs out records ZERO_DEVICE_TIMEOUT in g_zf_device_status, tells the
-// rest of the CTA to stop, and the CTA waits (bounded again) for the copies it
+// that runs out records kDeviceTimeout in g_zf_device_status, tells the rest
+// of the CTA to stop, and the CTA waits (bounded again) for the copies it
 // issued before it returns.
 #include "zero_kernels.cuh"
 
@@ -30,17 +39,19 @@ __device__ int g_zf_device_status = 0;
 
 namespace {
 
-constexpr int kStages = 6;                             // ring depth: 6 x 32 KB per SM
-constexpr int kConsumerWarps = kThreads / 32;          // 8 warps, 8 elements per thread
-constexpr int kTmaThreads = kThreads + 32;             // + 1 producer warp
-constexpr int kSliceElems = kTile + 8;                 // aligned superset of a rank's tile slice
-constexpr int kSliceBytes = kSliceElems * 2;           // 4112
+constexpr int kConsumerWarps = 16;                     // 512 consumers, 8 elements each
+constexpr int kConsumers = kConsumerWarps * 32;
+constexpr int kTmaThreads = kConsumers + 32;           // + 1 producer warp
+constexpr int kSliceElems = kStagedTile + 8;           // aligned superset of a rank's tile slice
+constexpr int kSliceBytes = kSliceElems * 2;           // 8208
 constexpr int kRanksPerStage = 8;
-constexpr int kStageBytes = kRanksPerStage * kSliceBytes;  // 32896 (>= 4 fp32 state arrays)
-constexpr int kStateArrayBytes = kTile * 4;            // 8192
+constexpr int kStageBytes = kRanksPerStage * kSliceBytes;  // 65664 (>= 4 fp32 state arrays)
+constexpr int kStages = 3;                             // ring depth: 3 x 64 KB per SM
+constexpr int kStateArrayBytes = kStagedTile * 4;      // 16384
 constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;       // 0.2 s
 
+static_assert(kConsumers * kVec == kStagedTile, "one thread owns 8 elements of a tile");
 static_assert(4 * kStateArrayBytes <= kStageBytes, "state block must fit one stage");
 static_assert(kSliceBytes % 16 == 0, "bulk copies need 16-byte sizes");
 
@@ -106,11 +117,26 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
     }
 }
 
+// Unit of a global tile index: the last unit whose first tile is <= tile.
+__device__ __forceinline__ int find_unit(const MultiArgs& a, int tile) {
+    int lo = 0, hi = a.n_units - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a.unit[mid].tile_begin <= tile) {
+            lo = mid;
+        } else {
+            hi = mid - 1;
+        }
+    }
+    return lo;
+}
+
 // Geometry of one tile, identical for the producer and the consumers.
 struct TileGeom {
-    int r;
+    const UnitDesc* u;
+    int r;            // rank whose shard the tile covers
     int64_t j0;       // first shard-local element of the tile
-    int nvalid;       // valid elements in the tile (<= kTile)
+    int nvalid;       // valid elements in the tile (<= kStagedTile)
     int64_t e0;       // first flat element
     int mis;          // e0 mod 8
     int64_t a0;       // aligned start of every rank's copied slice
@@ -118,22 +144,33 @@ struct TileGeom {
     int state_valid;  // state elements copied (multiple of 4)
 };
 
-__device__ __forceinline__ TileGeom tile_geom(int tile, int tiles_per_rank, int64_t S,
-                                              int64_t P_pad) {
+__device__ __forceinline__ TileGeom tile_geom(const MultiArgs& a, int tile) {
     TileGeom g;
-    g.r = tile / tiles_per_rank;
-    g.j0 = static_cast<int64_t>(tile - g.r * tiles_per_rank) * kTile;
+    g.u = &a.unit[find_unit(a, tile)];
+    const int local = tile - g.u->tile_begin;
+    const int64_t S = g.u->S;
+    g.r = local / g.u->tiles_per_rank;
+    g.j0 = static_cast<int64_t>(local - g.r * g.u->tiles_per_rank) * kStagedTile;
     const int64_t rem = S - g.j0;
-    g.nvalid = static_cast<int>(rem < kTile ? rem : kTile);
+    g.nvalid = static_cast<int>(rem < kStagedTile ? rem : kStagedTile);
     g.e0 = static_cast<int64_t>(g.r) * S + g.j0;
     g.mis = static_cast<int>(g.e0 & 7);
     g.a0 = g.e0 - g.mis;
-    int64_t a1 = (g.e0 + g.nvalid + 7) & ~static_cast<int64_t>(7);
-    const int64_t floor8 = P_pad & ~static_cast<int64_t>(7);
+    const int64_t a1 = (g.e0 + g.nvalid + 7) & ~static_cast<int64_t>(7);
+    const int64_t floor8 = g.u->P_pad & ~static_cast<int64_t>(7);
     g.a1 = a1 < floor8 ? a1 : floor8;
     if (g.a1 < g.a0) g.a1 = g.a0;
     g.state_valid = g.nvalid & ~3;
     return g;
+}
+
+template <typename T>
+__device__ __forceinline__ T ptr_at(const MultiArgs& a, int index) {
+    return static_cast<T>(const_cast<void*>(a.ptrs[index]));
+}
+
+__device__ __forceinline__ const uint16_t* grad_ptr(const MultiArgs& a, const UnitDesc* u, int k) {
+    return ptr_at<const uint16_t*>(a, u->off_grads + k);
 }
 
 template <int MODE>
@@ -147,17 +184,24 @@ template <> struct ModeTraits<kModeRsStore> { static constexpr int kStateArrays 
 // reduce-scatter adding the mean to the accumulator: state = accumulator
 template <> struct ModeTraits<kModeRsAdd> { static constexpr int kStateArrays = 1; };
 
-template <int MAXR, int MODE>
-__device__ __forceinline__ const float* state_src(const StepArgs<MAXR>& a, int array, int r) {
-    if constexpr (MODE == kModeRsAdd) {
-        return a.accum[r];
+// State array `array` of rank r (order: master, m, v, accumulator; the
+// reduce-scatter modes only have the accumulator).
+template <int MODE>
+__device__ __forceinline__ float* state_ptr(const MultiArgs& a, const UnitDesc* u, int array,
+                                            int r) {
+    if constexpr (MODE == kModeRsAdd || MODE == kModeRsStore) {
+        return ptr_at<float*>(a, u->off_accum + r);
     } else {
-        return array == 0 ? a.master[r] : array == 1 ? a.m[r] : array == 2 ? a.v[r] : a.accum[r];
+        const int off = array == 0 ? u->off_master
+                        : array == 1 ? u->off_m
+                        : array == 2 ? u->off_v
+                                     : u->off_accum;
+        return ptr_at<float*>(a, off + r);
     }
 }
 
-// Sum 1..kRanksPerStage rank slices of one stage into (s, c) for a thread's 8
-// elements starting A elements into its aligned pair of 16-byte words.
+// Sum up to kRanksPerStage rank slices of one stage into (s, c) for a
+// thread's 8 elements starting A elements into its aligned pair of words.
 template <int A>
 __device__ __forceinline__ void consume_stage(const uint8_t* stage, int nk, int tid,
                                               float2 (&s)[4], float2 (&c)[4]) {
@@ -173,15 +217,14 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage, int nk, int 
     }
 }
 
-template <int MAXR, int MODE>
-__device__ void producer_loop(const StepArgs<MAXR>& a, uint8_t* smem, uint64_t* full,
-                              uint64_t* empty, volatile int* abort_flag, uint32_t* issued_out) {
+template <int MODE>
+__device__ void producer_loop(const MultiArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
+                              volatile int* abort_flag, uint32_t* issued_out) {
     constexpr int NS = ModeTraits<MODE>::kStateArrays;
-    const int n_tiles = a.tiles_per_rank * a.n_ranks;
-    const int groups = (a.n_ranks + kRanksPerStage - 1) / kRanksPerStage;
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-        const TileGeom g = tile_geom(tile, a.tiles_per_rank, a.S, a.P_pad);
+    for (int tile = blockIdx.x; tile < a.total_tiles; tile += gridDim.x) {
+        const TileGeom g = tile_geom(a, tile);
+        const int n_ranks = g.u->n_ranks;
         if constexpr (NS > 0) {
             const uint32_t slot = it % kStages, parity = ((it / kStages) & 1) ^ 1;
             if (!mbar_wait_bounded(smem_u32(&empty[slot]), parity, abort_flag, kWaitLimitNs)) break;
@@ -193,48 +236,51 @@ __device__ void producer_loop(const StepArgs<MAXR>& a, uint8_t* smem, uint64_t* 
 #pragma unroll
                 for (int arr = 0; arr < NS; ++arr) {
                     bulk_copy_g2s(dst + arr * kStateArrayBytes,
-                                  state_src<MAXR, MODE>(a, arr, g.r) + g.j0, bytes, bar);
+                                  state_ptr<MODE>(a, g.u, arr, g.r) + g.j0, bytes, bar);
                 }
             }
             ++it;
         }
         const uint32_t gbytes = static_cast<uint32_t>(g.a1 - g.a0) * 2;
+        const int groups = (n_ranks + kRanksPerStage - 1) / kRanksPerStage;
+        bool stop = false;
         for (int grp = 0; grp < groups; ++grp) {
             const uint32_t slot = it % kStages, parity = ((it / kStages) & 1) ^ 1;
             if (!mbar_wait_bounded(smem_u32(&empty[slot]), parity, abort_flag, kWaitLimitNs)) {
-                *issued_out = it;
-                return;
+                stop = true;
+                break;
             }
             const int k0 = grp * kRanksPerStage;
-            const int nk = min(kRanksPerStage, a.n_ranks - k0);
+            const int nk = min(kRanksPerStage, n_ranks - k0);
             const uint32_t bar = smem_u32(&full[slot]);
             mbar_arrive_expect_tx(bar, nk * gbytes);
             if (gbytes > 0) {
                 const uint32_t dst = smem_u32(smem + slot * kStageBytes);
                 for (int kk = 0; kk < nk; ++kk) {
-                    bulk_copy_g2s(dst + kk * kSliceBytes, a.grads[k0 + kk] + g.a0, gbytes, bar);
+                    bulk_copy_g2s(dst + kk * kSliceBytes, grad_ptr(a, g.u, k0 + kk) + g.a0, gbytes,
+                                  bar);
                 }
             }
             ++it;
         }
-        if (*abort_flag) break;
+        if (stop || *abort_flag) break;
     }
     *issued_out = it;
 }
 
-template <int MAXR, int MODE>
-__device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint64_t* full,
+template <int MODE>
+__device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t* full,
                               uint64_t* empty, volatile int* abort_flag,
                               unsigned int* consumed_min) {
     constexpr int NS = ModeTraits<MODE>::kStateArrays;
-    const int tid = threadIdx.x;  // 0..kThreads-1
+    const int tid = threadIdx.x;  // 0..kConsumers-1
     const int lane = tid & 31;
-    const int n_tiles = a.tiles_per_rank * a.n_ranks;
-    const int groups = (a.n_ranks + kRanksPerStage - 1) / kRanksPerStage;
     uint32_t it = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
-        const TileGeom g = tile_geom(tile, a.tiles_per_rank, a.S, a.P_pad);
+    for (int tile = blockIdx.x; tile < a.total_tiles && ok; tile += gridDim.x) {
+        const TileGeom g = tile_geom(a, tile);
+        const UnitDesc* u = g.u;
+        const int n_ranks = u->n_ranks;
         const int first = tid * kVec;
         const int nv = max(0, min(kVec, g.nvalid - first));
         const int64_t j = g.j0 + first;       // thread's first shard-local element
@@ -257,7 +303,7 @@ __device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint
                     st[arr][0] = x0.x; st[arr][1] = x0.y; st[arr][2] = x0.z; st[arr][3] = x0.w;
                     st[arr][4] = x1.x; st[arr][5] = x1.y; st[arr][6] = x1.z; st[arr][7] = x1.w;
                 } else {
-                    const float* src = state_src<MAXR, MODE>(a, arr, g.r) + j;
+                    const float* src = state_ptr<MODE>(a, u, arr, g.r) + j;
 #pragma unroll
                     for (int t = 0; t < kVec; ++t) st[arr][t] = (t < nv) ? src[t] : 0.0f;
                 }
@@ -273,10 +319,8 @@ __device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint
             s[q] = make_float2(0.0f, 0.0f);
             c[q] = make_float2(0.0f, 0.0f);
         }
-        float ss[8], cs[8];
-#pragma unroll
-        for (int t = 0; t < kVec; ++t) ss[t] = cs[t] = 0.0f;
         const bool vec = (nv == kVec) && (e + kVec <= g.a1);
+        const int groups = (n_ranks + kRanksPerStage - 1) / kRanksPerStage;
         for (int grp = 0; grp < groups; ++grp) {
             const uint32_t slot = it % kStages, parity = (it / kStages) & 1;
             if (!mbar_wait_bounded(smem_u32(&full[slot]), parity, abort_flag, kWaitLimitNs)) {
@@ -284,7 +328,7 @@ __device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint
                 break;
             }
             const int k0 = grp * kRanksPerStage;
-            const int nk = min(kRanksPerStage, a.n_ranks - k0);
+            const int nk = min(kRanksPerStage, n_ranks - k0);
             const uint8_t* stage = smem + slot * kStageBytes;
             if (vec) {
                 switch (g.mis) {
@@ -298,11 +342,16 @@ __device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint
                     default: consume_stage<7>(stage, nk, tid, s, c); break;
                 }
             } else if (nv > 0) {
+                // Ragged end: scalar reads from global memory, the same two-sum
+                // lane by lane (element 2q in .x, 2q+1 in .y).
                 for (int kk = 0; kk < nk; ++kk) {
-                    const uint16_t* src = a.grads[k0 + kk] + e;
+                    const uint16_t* src = grad_ptr(a, u, k0 + kk) + e;
 #pragma unroll
-                    for (int t = 0; t < kVec; ++t) {
-                        if (t < nv) two_sum_add1(ss[t], cs[t], bf16_to_float(src[t]));
+                    for (int q = 0; q < 4; ++q) {
+                        if (2 * q < nv) two_sum_add1(s[q].x, c[q].x, bf16_to_float(src[2 * q]));
+                        if (2 * q + 1 < nv) {
+                            two_sum_add1(s[q].y, c[q].y, bf16_to_float(src[2 * q + 1]));
+                        }
                     }
                 }
             }
@@ -313,18 +362,10 @@ __device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint
         if (!ok || nv == 0) continue;
 
         float mean[8];
-        if (vec) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                mean[2 * q] = finish_mean(s[q].x, c[q].x, a.n_ranks_f, a.inv_n, a.n_pow2);
-                mean[2 * q + 1] = finish_mean(s[q].y, c[q].y, a.n_ranks_f, a.inv_n, a.n_pow2);
-            }
-        } else {
-#pragma unroll
-            for (int t = 0; t < kVec; ++t) {
-                mean[t] = (t < nv) ? finish_mean(ss[t], cs[t], a.n_ranks_f, a.inv_n, a.n_pow2)
-                                   : 0.0f;
-            }
+        for (int q = 0; q < 4; ++q) {
+            mean[2 * q] = finish_mean(s[q].x, c[q].x, u->n_ranks_f, u->inv_n, u->n_pow2);
+            mean[2 * q + 1] = finish_mean(s[q].y, c[q].y, u->n_ranks_f, u->inv_n, u->n_pow2);
         }
 
         if constexpr (MODE == kModeRsStore || MODE == kModeRsAdd) {
@@ -334,7 +375,7 @@ __device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint
                 out[t] = mean[t];
                 if constexpr (MODE == kModeRsAdd) out[t] = __fadd_rn(st[0][t], mean[t]);
             }
-            float* dst = a.accum[g.r] + j;
+            float* dst = state_ptr<MODE>(a, u, 0, g.r) + j;
             if (nv == kVec) {
                 st_f32x8(dst, out);
             } else {
@@ -349,23 +390,30 @@ __device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint
                 }
                 adamw_update(a.k, gr, st[0][t], st[1][t], st[2][t]);
             }
+            float* master = state_ptr<MODE>(a, u, 0, g.r) + j;
+            float* m = state_ptr<MODE>(a, u, 1, g.r) + j;
+            float* v = state_ptr<MODE>(a, u, 2, g.r) + j;
             if (nv == kVec) {
-                st_f32x8(a.master[g.r] + j, st[0]);
-                st_f32x8(a.m[g.r] + j, st[1]);
-                st_f32x8(a.v[g.r] + j, st[2]);
+                st_f32x8(master, st[0]);
+                st_f32x8(m, st[1]);
+                st_f32x8(v, st[2]);
                 const uint4 w = make_uint4(pack_bf16x2(st[0][0], st[0][1]),
                                            pack_bf16x2(st[0][2], st[0][3]),
                                            pack_bf16x2(st[0][4], st[0][5]),
                                            pack_bf16x2(st[0][6], st[0][7]));
                 const int mis = static_cast<int>(e & 7);
-                for (int o = 0; o < a.n_out; ++o) store_bf16x8(a.out[o], e, mis, w);
+                for (int o = 0; o < u->n_out; ++o) {
+                    store_bf16x8(ptr_at<uint16_t*>(a, u->off_out + o), e, mis, w);
+                }
             } else {
                 for (int t = 0; t < nv; ++t) {
-                    a.master[g.r][j + t] = st[0][t];
-                    a.m[g.r][j + t] = st[1][t];
-                    a.v[g.r][j + t] = st[2][t];
+                    master[t] = st[0][t];
+                    m[t] = st[1][t];
+                    v[t] = st[2][t];
                     const uint16_t b = float_to_bf16_rn(st[0][t]);
-                    for (int o = 0; o < a.n_out; ++o) a.out[o][e + t] = b;
+                    for (int o = 0; o < u->n_out; ++o) {
+                        ptr_at<uint16_t*>(a, u->off_out + o)[e + t] = b;
+                    }
                 }
             }
         }
@@ -375,9 +423,9 @@ __device__ void consumer_loop(const StepArgs<MAXR>& a, const uint8_t* smem, uint
 
 }  // namespace
 
-template <int MAXR, int MODE>
+template <int MODE>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-staged_step_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+staged_step_kernel(const __grid_constant__ MultiArgs a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[kStages];
     __shared__ __align__(8) uint64_t empty[kStages];
@@ -396,12 +444,10 @@ staged_step_kernel(const __grid_constant__ StepArgs<MAXR> a) {
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
-    if (threadIdx.x >= kThreads) {
-        if (threadIdx.x == kThreads) {
-            producer_loop<MAXR, MODE>(a, smem, full, empty, &abort_flag, &issued);
-        }
+    if (threadIdx.x >= kConsumers) {
+        if (threadIdx.x == kConsumers) producer_loop<MODE>(a, smem, full, empty, &abort_flag, &issued);
     } else {
-        consumer_loop<MAXR, MODE>(a, smem, full, empty, &abort_flag, &consumed_min);
+        consumer_loop<MODE>(a, smem, full, empty, &abort_flag, &consumed_min);
     }
     __syncthreads();
     if (threadIdx.x == 0 && abort_flag) {
@@ -414,26 +460,25 @@ staged_step_kernel(const __grid_constant__ StepArgs<MAXR> a) {
     }
 }
 
-template <int MAXR, int MODE>
-static cudaError_t launch_staged(const StepArgs<MAXR>& a, cudaStream_t stream) {
-    const void* kfn = reinterpret_cast<const void*>(&staged_step_kernel<MAXR, MODE>);
+template <int MODE>
+static cudaError_t launch_staged(const MultiArgs& a, cudaStream_t stream) {
+    const void* kfn = reinterpret_cast<const void*>(&staged_step_kernel<MODE>);
     const size_t smem = static_cast<size_t>(kStages) * kStageBytes;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int64_t n_tiles = static_cast<int64_t>(a.tiles_per_rank) * a.n_ranks;
-    const int grid = persistent_grid(kfn, kTmaThreads, smem, n_tiles);
-    staged_step_kernel<MAXR, MODE><<<grid, kTmaThreads, smem, stream>>>(a);
+    const int grid = persistent_grid(kfn, kTmaThreads, smem, a.total_tiles);
+    staged_step_kernel<MODE><<<grid, kTmaThreads, smem, stream>>>(a);
     return cudaGetLastError();
 }
 
-template <int MAXR>
-cudaError_t launch_staged_step(const StepArgs<MAXR>& a, int mode, cudaStream_t stream) {
+cudaError_t launch_staged_step(const MultiArgs& a, int mode, cudaStream_t stream) {
+    if (a.total_tiles <= 0) return cudaSuccess;
     switch (mode) {
-        case kModePlain: return launch_staged<MAXR, kModePlain>(a, stream);
-        case kModeAccumFinal: return launch_staged<MAXR, kModeAccumFinal>(a, stream);
-        case kModeRsStore: return launch_staged<MAXR, kModeRsStore>(a, stream);
-        default: return launch_staged<MAXR, kModeRsAdd>(a, stream);
+        case kModePlain: return launch_staged<kModePlain>(a, stream);
+        case kModeAccumFinal: return launch_staged<kModeAccumFinal>(a, stream);
+        case kModeRsStore: return launch_staged<kModeRsStore>(a, stream);
+        default: return launch_staged<kModeRsAdd>(a, stream);
     }
 }
 
@@ -470,8 +515,5 @@ cudaError_t read_device_status(int* status, int clear, cudaStream_t stream) {
     *status = v;
     return e;
 }
-
-template cudaError_t launch_staged_step<64>(const StepArgs<64>&, int, cudaStream_t);
-template cudaError_t launch_staged_step<512>(const StepArgs<512>&, int, cudaStream_t);
 
 }  // namespace zf

@@ -42,6 +42,14 @@ class ZeroLayout(ctypes.Structure):
                 f"n_ranks={self.n_ranks})")
 
 
+class ZeroUnit(ctypes.Structure):
+    """zero_unit_t: one FlatParameter's layout and buffers for zero_step_units."""
+    _fields_ = [("layout", ctypes.POINTER(ZeroLayout)), ("grads", ctypes.c_void_p),
+                ("master", ctypes.c_void_p), ("m", ctypes.c_void_p), ("v", ctypes.c_void_p),
+                ("accum", ctypes.c_void_p), ("full_params", ctypes.c_void_p),
+                ("n_out", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 class ZeroAdamW(ctypes.Structure):
     """zero_adamw_t: hyper-parameters of one AdamW step (t >= 1)."""
     _fields_ = [("lr", ctypes.c_double), ("beta1", ctypes.c_double),
@@ -84,6 +92,8 @@ def load() -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        lib.zero_step_units.argtypes = [ctypes.POINTER(ZeroUnit), i32, i32, i32, hp, p]
+        lib.zero_step_units.restype = ctypes.c_int
         lib.zero_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_int32), i32]
         lib.zero_device_status.restype = ctypes.c_int
         lib.zero_selftest_wait_timeout.argtypes = [i64, p]
@@ -244,3 +254,24 @@ def zero_selftest_wait_timeout(limit_ns: int, stream=None):
     """Launch a kernel whose bounded barrier wait must run out after limit_ns."""
     _check(load().zero_selftest_wait_timeout(int(limit_ns), _stream(stream)),
            "zero_selftest_wait_timeout")
+
+
+def zero_step_units(units, micro_step: int, n_micro: int, hp, stream=None):
+    """units: sequence of (grads, master, m, v, accum or None, full_params, layout)."""
+    n = len(units)
+    arr = (ZeroUnit * max(n, 1))()
+    keep = []
+    for i, (grads, master, m, v, accum, full, layout) in enumerate(units):
+        tabs = [_ptrs(grads), _ptrs(master), _ptrs(m), _ptrs(v),
+                _ptrs(accum) if accum is not None else None, _ptrs(full)]
+        keep.append((tabs, layout))
+        arr[i].layout = ctypes.pointer(layout)
+        arr[i].grads, arr[i].master, arr[i].m, arr[i].v = (ctypes.cast(t, ctypes.c_void_p)
+                                                           for t in tabs[:4])
+        arr[i].accum = ctypes.cast(tabs[4], ctypes.c_void_p) if tabs[4] is not None else None
+        arr[i].full_params = ctypes.cast(tabs[5], ctypes.c_void_p)
+        arr[i].n_out = len(full)
+    h = _hp(hp)
+    _check(load().zero_step_units(arr, n, int(micro_step), int(n_micro),
+                                  ctypes.byref(h) if h is not None else None, _stream(stream)),
+           "zero_step_units")

@@ -229,6 +229,36 @@ int zero_device_status(void* stream, int32_t* status, int32_t clear);
  */
 int zero_selftest_wait_timeout(int64_t limit_ns, void* stream);
 
+/*
+ * zero_unit_t / zero_step_units -- device, fused, several FlatParameters per
+ * launch.  FSDP wraps a model as many units (one per transformer block plus a
+ * root unit, [LA] section 9.1; [DZ] section 5.5), each its own FlatParameter
+ * with its own layout and buffers.  zero_step_units(units, n) computes exactly
+ * what n calls of zero_step (one per unit, same micro_step / n_micro / hp)
+ * compute, bit for bit, but packs the units into as few launches as the launch
+ * argument block allows (up to 32 units and 3712 pointers per launch), so
+ * small units do not each pay a launch, a pipeline fill and a tail.
+ * Either every unit has an accumulator or none does.
+ */
+#define ZERO_UNITS_PER_LAUNCH 32      /* units packed into one launch at most          */
+#define ZERO_POINTERS_PER_LAUNCH 3712 /* device pointers per launch: per unit 4*N_d +    */
+                                      /* n_out (plain), 5*N_d + n_out (last micro-step), */
+                                      /* 2*N_d (accumulation micro-step)                 */
+typedef struct zero_unit {
+    const zero_layout_t* layout;
+    const uint16_t* const* grads;    /* [layout->n_ranks] bf16, each P_pad   */
+    float* const* master;            /* [n_ranks] fp32, each S               */
+    float* const* m;                 /* [n_ranks]                            */
+    float* const* v;                 /* [n_ranks]                            */
+    float* const* accum;             /* [n_ranks] or NULL                    */
+    uint16_t* const* full_params;    /* [n_out] bf16, each P_pad             */
+    int32_t n_out;
+    int32_t reserved;
+} zero_unit_t;
+
+int zero_step_units(const zero_unit_t* units, int32_t n_units, int32_t micro_step,
+                    int32_t n_micro, const zero_adamw_t* hp, void* stream);
+
 /* Message for the last non-OK return on the calling thread ("" if none). */
 const char* zero_last_error(void);
 

@@ -238,3 +238,71 @@ def test_misaligned_pointer_rejected_without_launch():
     with pytest.raises(zf.ZeroError) as ei:
         zf.zero_step(bad, *u.state_rows(), None, 1, 1, u.param_rows(), u.layout, hp_at(1))
     assert ei.value.code == -2
+
+
+def _units(specs, n_out=1, accum=False, tag="units"):
+    out = []
+    for i, (numels, n_ranks) in enumerate(specs):
+        u = FlatUnit(numels, n_ranks, n_out=n_out, accum=accum)
+        u.set_master_flat(synthetic.make_master_flat(u.P, n_ranks, 0.02, (tag, i)).cuda())
+        out.append(u)
+    return out
+
+
+def _unit_tuple(u, accum):
+    return (u.grad_rows(), *u.state_rows(), u.accum_rows() if accum else None, u.param_rows(),
+            u.layout)
+
+
+@pytest.mark.parametrize("n_micro", [1, 3])
+@pytest.mark.parametrize("specs", [
+    # GPT-2-small-like: 12 equal blocks + a bigger root unit (scaled down), N_d = 8
+    [([768, 768, 9000, 300], 8)] * 12 + [([50000, 7000, 5], 8)],
+    # more units than fit one launch, mixed rank counts and ragged shards
+    [([1000 + 37 * i], 1 + (i % 9)) for i in range(40)],
+    # pointer-limited packing: 64 ranks per unit -> at most 14 units per launch
+    [([64 * 53 + i], 64) for i in range(20)],
+], ids=["gpt2_like", "40_units_mixed", "pointer_limited"])
+def test_step_units_equals_per_unit_steps(kernel, specs, n_micro):
+    """zero_step_units over many FlatParameters is bit-identical to one
+    zero_step per unit."""
+    acc = n_micro > 1
+    a_units = _units(specs, n_out=2, accum=acc)
+    b_units = _units(specs, n_out=2, accum=acc)
+    for t in (1, 2):
+        for k in range(1, n_micro + 1):
+            for i, (a, b) in enumerate(zip(a_units, b_units)):
+                g = synthetic.make_grads(a.P, a.n_ranks, 1e-2, ("su", i, t, k)).cuda()
+                a.grads.copy_(g)
+                b.grads.copy_(g)
+            zf.zero_step_units([_unit_tuple(a, acc) for a in a_units], k, n_micro, hp_at(t))
+            for b in b_units:
+                zf.zero_step(b.grad_rows(), *b.state_rows(), b.accum_rows() if acc else None, k,
+                             n_micro, b.param_rows(), b.layout, hp_at(t))
+    torch.cuda.synchronize()
+    for a, b in zip(a_units, b_units):
+        for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+            assert torch.equal(x.contiguous().view(torch.int32), y.contiguous().view(torch.int32))
+        assert torch.equal(a.params.contiguous().view(torch.int16),
+                           b.params.contiguous().view(torch.int16))
+
+
+def test_step_units_against_oracle(oracle):
+    """Three units of different shapes stepped together, each checked against
+    the oracle."""
+    cases = [Case([4099, 17], 4, tag="su0"), Case([100003], 8, tag="su1"),
+             Case([64 * 77 + 3], 64, tag="su2")]
+    for t in (1, 2, 3):
+        grads = []
+        for c in cases:
+            g = c.grads_for(t, 1)
+            c.unit.grads.copy_(g.cuda())
+            grads.append(g)
+        zf.zero_step_units([_unit_tuple(c.unit, False) for c in cases], 1, 1, hp_at(t))
+        for c, g in zip(cases, grads):
+            hp = hp_at(t)
+            c.o_params = oracle.zero_step(bits(g), c.o_master, c.o_m, c.o_v, lr=hp["lr"],
+                                          beta1=hp["beta1"], beta2=hp["beta2"], eps=hp["eps"],
+                                          weight_decay=hp["weight_decay"], step=t)
+    for c in cases:
+        c.compare()
