@@ -70,6 +70,12 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_adamw.restype = None
     lib.oracle_all_gather.argtypes = [p, i32, i64, p]
     lib.oracle_all_gather.restype = None
+    lib.oracle_sum_squares.argtypes = [p, i64]
+    lib.oracle_sum_squares.restype = f64
+    lib.oracle_clip_coefficient.argtypes = [f64, f64]
+    lib.oracle_clip_coefficient.restype = ctypes.c_float
+    lib.oracle_scale.argtypes = [p, i64, ctypes.c_float]
+    lib.oracle_scale.restype = None
     lib.oracle_zero_step.argtypes = [p, p, p, p, p, i32, i32, p, i32, i64,
                                      f64, f64, f64, f64, f64, i64]
     lib.oracle_zero_step.restype = ctypes.c_int
@@ -193,6 +199,63 @@ class Oracle:
             _f32(a)
         self.lib.oracle_adamw(_ptr(theta), _ptr(m), _ptr(v), _ptr(np.ascontiguousarray(g)),
                               theta.size, lr, beta1, beta2, eps, weight_decay, int(step))
+
+    # -- gradient clipping ----------------------------------------------
+    def sum_squares(self, g) -> float:
+        g = _f32(g)
+        return float(self.lib.oracle_sum_squares(_ptr(g), g.size))
+
+    def clip_coefficient(self, total_sum_squares: float, max_norm: float) -> np.float32:
+        return np.float32(self.lib.oracle_clip_coefficient(float(total_sum_squares),
+                                                           float(max_norm)))
+
+    def scale(self, g, coef) -> None:
+        g = _f32(g)
+        self.lib.oracle_scale(_ptr(g), g.size, float(coef))
+
+    def averaged_gradient(self, grads, accum=None, micro_step: int = 1, n_micro: int = 1):
+        """The gradient one unit's optimizer step uses: the reduce-scatter mean,
+        or, at the last of n_micro micro-steps, the accumulated mean / n_micro.
+        grads: (n_ranks, P_pad) uint16 -> (n_ranks, S) float32 (None for an
+        accumulation-only micro-step)."""
+        g = self.reduce_scatter(grads)
+        if accum is not None and n_micro > 1:
+            self.accumulate(accum, g, micro_step == 1)
+            if micro_step < n_micro:
+                return None
+            g = self.average_micro(accum, n_micro)
+        return g
+
+    def clipped_units_step(self, units, *, max_norm, lr, beta1, beta2, eps, weight_decay, step,
+                           micro_step: int = 1, n_micro: int = 1):
+        """One step over several units with global gradient-norm clipping.
+
+        units: list of dicts with 'grads' (n_ranks, P_pad) uint16 and 'master',
+        'm', 'v' (and 'accum' when micro-stepping) (n_ranks, S) float32,
+        updated in place.  Steps: every unit's averaged gradient; the norm over
+        all of them; the common clip coefficient; AdamW on each rank's shard
+        with the scaled gradient; bf16 cast; all-gather.  Returns (list of
+        gathered bf16 buffers or None, total norm, coefficient).
+        """
+        gs = [self.averaged_gradient(u["grads"], u.get("accum"), micro_step, n_micro)
+              for u in units]
+        if gs[0] is None:
+            return None, None, None
+        total = 0.0
+        for g in gs:
+            total = total + self.sum_squares(g)
+        coef = self.clip_coefficient(total, max_norm)
+        outs = []
+        for u, g in zip(units, gs):
+            self.scale(g, coef)
+            n_ranks = g.shape[0]
+            shards = np.empty(g.shape, dtype=np.uint16)
+            for r in range(n_ranks):
+                self.adamw(u["master"][r], u["m"][r], u["v"][r], g[r], lr=lr, beta1=beta1,
+                           beta2=beta2, eps=eps, weight_decay=weight_decay, step=step)
+                shards[r] = self.round_to_bf16(u["master"][r])
+            outs.append(self.all_gather(shards))
+        return outs, float(np.sqrt(total)), coef
 
     def zero_step(self, grads, master, m, v, *, lr, beta1, beta2, eps, weight_decay, step,
                   accum=None, micro_step: int = 1, n_micro: int = 1):

@@ -230,6 +230,49 @@ void oracle_adamw(float* theta, float* m, float* v, const float* g, int64_t n, d
     }
 }
 
+/* ------------------------------------------------ gradient clipping ------- */
+
+/*
+ * Global gradient-norm clipping ([DZ] section 6: a global norm needs a
+ * reduction across every shard).  Reading: the clip-by-total-L2-norm rule of
+ * data-parallel training -- the norm is taken over the averaged gradient of
+ * every element of every unit, coef = max_norm / (norm + 1e-6), and the
+ * gradient is multiplied by coef only when coef < 1.
+ */
+
+/* Sum of squares of n fp32 values, in double. */
+double oracle_sum_squares(const float* g, int64_t n)
+{
+    double acc = 0.0;
+    for (int64_t i = 0; i < n; ++i) {
+        acc = acc + (double)g[i] * (double)g[i];
+    }
+    return acc;
+}
+
+/* The clip coefficient from the total sum of squares, rounded once to fp32
+ * (the gradient it multiplies is fp32); 1 when no clipping is needed. */
+float oracle_clip_coefficient(double total_sum_squares, double max_norm)
+{
+    double norm = sqrt(total_sum_squares);
+    double coef = max_norm / (norm + 1e-6);
+    if (coef >= 1.0) {
+        return 1.0f;
+    }
+    return (float)coef;
+}
+
+/* g = fp32(g * coef), in place (left unchanged when coef == 1). */
+void oracle_scale(float* g, int64_t n, float coef)
+{
+    if (coef == 1.0f) {
+        return;
+    }
+    for (int64_t i = 0; i < n; ++i) {
+        g[i] = (float)((double)g[i] * (double)coef);
+    }
+}
+
 /* --------------------------------------------------------- all-gather ----- */
 
 /*

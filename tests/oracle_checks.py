@@ -398,6 +398,94 @@ def check_accumulation_invariants(o):
     assert np.array_equal(outs[0][2].reshape(-1), ref_m)
 
 
+def check_clip_coefficient_vs_torch(o):
+    """The clip coefficient and the clipped gradients against
+    torch.nn.utils.clip_grad_norm_ (a library routine), at norms where the
+    1e-6 in the denominator matters and where clipping does not apply."""
+    rng = np.random.default_rng(12)
+    for scale, max_norm in ((1e-4, 1e-5), (1e-2, 0.05), (1.0, 1e3), (1e-3, 7e-4)):
+        parts = [rng.normal(0, scale, n).astype(np.float32) for n in (17, 300, 1)]
+        params = [torch.nn.Parameter(torch.zeros(len(x))) for x in parts]
+        for p, x in zip(params, parts):
+            p.grad = torch.from_numpy(x.copy())
+        tnorm = float(torch.nn.utils.clip_grad_norm_(params, max_norm))
+        total = sum(o.sum_squares(x) for x in parts)
+        assert abs(np.sqrt(total) - tnorm) <= 1e-6 * tnorm
+        coef = o.clip_coefficient(total, max_norm)
+        for p, x in zip(params, parts):
+            y = x.copy()
+            o.scale(y, coef)
+            ref = p.grad.numpy()
+            assert np.all(np.abs(y - ref) <= 2e-6 * np.abs(ref) + 1e-30)
+            if coef == 1.0:
+                assert np.array_equal(y, x)
+
+
+def check_clip_closed_forms(o):
+    """A constant gradient c over n elements has norm |c|*sqrt(n): coef =
+    max_norm / (|c| sqrt(n) + 1e-6) and the clipped norm is just under max_norm;
+    below the threshold the coefficient is exactly 1."""
+    g = np.full(64, 0.5, np.float32)          # norm exactly 4
+    total = o.sum_squares(g)
+    assert total == 16.0
+    coef = o.clip_coefficient(total, 2.0)
+    assert coef == np.float32(2.0 / (4.0 + 1e-6))
+    y = g.copy()
+    o.scale(y, coef)
+    assert np.sqrt(o.sum_squares(y)) == pytest_approx(2.0 * 4.0 / (4.0 + 1e-6), 1e-7)
+    assert o.clip_coefficient(total, 4.0 + 1e-5) == 1.0
+    assert o.clip_coefficient(0.0, 1.0) == 1.0
+
+
+def pytest_approx(x, rel):
+    import pytest
+    return pytest.approx(x, rel=rel)
+
+
+def check_clipped_units_step_vs_torch(o):
+    """N_d = 1, three units, ten steps: the oracle's clipped step against
+    torch.nn.utils.clip_grad_norm_ over all parameters followed by
+    torch.optim.AdamW (foreach=False); the norm spans every unit."""
+    rng = np.random.default_rng(13)
+    sizes = (33, 200, 7)
+    units = []
+    for n in sizes:
+        theta0 = rng.normal(0, 0.02, n).astype(np.float32)
+        units.append(dict(master=theta0.reshape(1, n).copy(), m=np.zeros((1, n), np.float32),
+                          v=np.zeros((1, n), np.float32), theta0=theta0))
+    params = [torch.nn.Parameter(torch.from_numpy(u["theta0"].astype(np.float64).copy()))
+              for u in units]
+    opt = torch.optim.AdamW(params, lr=HP["lr"], betas=(HP["beta1"], HP["beta2"]),
+                            eps=HP["eps"], weight_decay=HP["weight_decay"], foreach=False)
+    max_norm = 5e-3
+    clipped_any = False
+    for t in range(1, 11):
+        for u, p in zip(units, params):
+            u["grads"] = random_bf16(rng, (1, u["master"].shape[1]), 1e-3)
+            p.grad = torch.from_numpy(bits_to_f32(u["grads"][0]).astype(np.float64))
+        outs, norm, coef = o.clipped_units_step(units, max_norm=max_norm, step=t, **HP)
+        clipped_any |= coef < 1.0
+        tnorm = float(torch.nn.utils.clip_grad_norm_(params, max_norm))
+        assert abs(norm - tnorm) <= 1e-9 * tnorm
+        # the method clips fp32 gradients: round torch's clipped grads to fp32
+        for p in params:
+            p.grad.copy_(torch.from_numpy(p.grad.numpy().astype(np.float32).astype(np.float64)))
+        opt.step()
+        with torch.no_grad():
+            for p in params:
+                st = opt.state[p]
+                p.copy_(torch.from_numpy(p.detach().numpy().astype(np.float32).astype(np.float64)))
+                for key in ("exp_avg", "exp_avg_sq"):
+                    st[key].copy_(torch.from_numpy(st[key].numpy().astype(np.float32)
+                                                   .astype(np.float64)))
+        for u, out in zip(units, outs):
+            assert np.array_equal(out, o.round_to_bf16(u["master"].reshape(-1)))
+    assert clipped_any
+    for u, p in zip(units, params):
+        ref = p.detach().numpy()
+        assert np.all(np.abs(u["master"][0] - ref) <= 2.0 ** -20 * (np.abs(ref) + HP["lr"]))
+
+
 ALL_CHECKS = [
     check_bf16_rounding,
     check_bf16_widening,
@@ -414,4 +502,7 @@ ALL_CHECKS = [
     check_adam_zero_gradient,
     check_single_rank_matches_torch_adamw,
     check_accumulation_invariants,
+    check_clip_coefficient_vs_torch,
+    check_clip_closed_forms,
+    check_clipped_units_step_vs_torch,
 ]

@@ -37,6 +37,10 @@ MUTANTS = {
                           "full[(int64_t)r * S + i] = shards[(int64_t)((r + 1) % n_ranks) * S + i];"),
     "accum_not_reset": ("if (first) {", "if (0) {"),
     "accum_no_average": ("(double)acc[i] / (double)n_micro", "(double)acc[i]"),
+    "clip_no_sqrt": ("double norm = sqrt(total_sum_squares);", "double norm = total_sum_squares;"),
+    "clip_no_clamp": ("if (coef >= 1.0) {", "if (coef >= 1e300) {"),
+    "clip_no_eps": ("double coef = max_norm / (norm + 1e-6);", "double coef = max_norm / norm;"),
+    "clip_scale_ignored": ("g[i] = (float)((double)g[i] * (double)coef);", "g[i] = g[i];"),
     "decay_after_update": ("double updated = decayed - lr * m_hat / (sqrt(v_hat) + eps);",
                            "double updated = ((double)theta[i] - lr * m_hat / (sqrt(v_hat) + eps)) * (1.0 - lr * weight_decay * 1.5);"),
 }
