@@ -91,10 +91,14 @@ def peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+KERNEL_SOURCES = ("zero_step_tma.cu", "zero_common.cuh", "zero_kernels.cuh")
+
+
 def kernel_source_hash() -> str:
+    """Hash of the sources of the timed kernel (staged fused step)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "fsdp_sharded_mixed_flatten_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]

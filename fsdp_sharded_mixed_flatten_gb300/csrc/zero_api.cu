@@ -153,19 +153,34 @@ struct UnitView {
     int32_t n_out;
 };
 
+bool mode_reads_grads(int mode) { return mode != zf::kModeFromShard; }
+bool mode_updates(int mode) {
+    return mode == zf::kModePlain || mode == zf::kModeAccumFinal || mode == zf::kModeFromShard;
+}
+bool mode_uses_accum(int mode) { return mode != zf::kModePlain; }
+
 int pointers_needed(const UnitView& u, int mode) {
     const int n = u.L->n_ranks;
-    switch (mode) {
-        case zf::kModePlain: return 4 * n + u.n_out;
-        case zf::kModeAccumFinal: return 5 * n + u.n_out;
-        default: return 2 * n;  // reduce-scatter: gradients + gradient-shard outputs
-    }
+    return (mode_reads_grads(mode) ? n : 0) + (mode_updates(mode) ? 3 * n + u.n_out : 0) +
+           (mode_uses_accum(mode) ? n : 0);
 }
+
+// Global gradient-norm clipping bookkeeping: where the norm launches write
+// their per-CTA partial sums and what the update launches reduce.
+struct ClipPlan {
+    double* partials = nullptr;
+    int64_t capacity = 0;     // slots available
+    int64_t slots_used = 0;   // written so far by norm launches
+    int32_t n_partials = 0;   // slots the update launches reduce
+    double max_norm = 0.0;
+    float* norm_out = nullptr;
+    bool dry_run = false;     // only count slots (no launch)
+};
 
 // Pack units into as few staged launches as the argument block allows
 // (kMaxUnits units, kMaxPtrs pointers) and launch them in order.
 int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::AdamConsts& k,
-                        cudaStream_t stream) {
+                        cudaStream_t stream, ClipPlan* clip = nullptr) {
     static thread_local zf::MultiArgs a;
     int np = 0;
     a.n_units = 0;
@@ -173,7 +188,26 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
     a.k = k;
     auto flush = [&]() -> int {
         if (a.n_units == 0) return ZERO_OK;
-        const int rc = cuda_status(zf::launch_staged_step(a, mode, stream), "staged step launch");
+        int rc = ZERO_OK;
+        if (clip != nullptr) {
+            a.partials = clip->partials;
+            a.partial_base = static_cast<int32_t>(clip->slots_used);
+            a.n_partials = clip->n_partials;
+            a.max_norm = clip->max_norm;
+            a.norm_out = clip->norm_out;
+            if (mode == zf::kModeRsNorm || mode == zf::kModeRsAvgNorm) {
+                const int grid = zf::staged_grid(mode, a.total_tiles);
+                if (clip->slots_used + grid > clip->capacity && !clip->dry_run)
+                    return fail(ZERO_ERR_SIZE, "clipping workspace too small: need %lld slots",
+                                (long long)(clip->slots_used + grid));
+                clip->slots_used += grid;
+            }
+        } else {
+            a.partials = nullptr;
+            a.norm_out = nullptr;
+        }
+        if (clip == nullptr || !clip->dry_run)
+            rc = cuda_status(zf::launch_staged_step(a, mode, stream), "staged step launch");
         a.n_units = 0;
         a.total_tiles = 0;
         np = 0;
@@ -199,10 +233,12 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
         d.n_ranks_f = static_cast<float>(n);
         d.inv_n = static_cast<float>(1.0 / static_cast<double>(n));
         d.n_pow2 = (n & (n - 1)) == 0 ? 1 : 0;
-        d.off_grads = np;
-        for (int r = 0; r < n; ++r) a.ptrs[np++] = u.grads[r];
-        d.off_master = d.off_m = d.off_v = d.off_accum = d.off_out = -1;
-        if (mode == zf::kModePlain || mode == zf::kModeAccumFinal) {
+        d.off_grads = d.off_master = d.off_m = d.off_v = d.off_accum = d.off_out = -1;
+        if (mode_reads_grads(mode)) {
+            d.off_grads = np;
+            for (int r = 0; r < n; ++r) a.ptrs[np++] = u.grads[r];
+        }
+        if (mode_updates(mode)) {
             d.off_master = np;
             for (int r = 0; r < n; ++r) a.ptrs[np++] = u.master[r];
             d.off_m = np;
@@ -213,7 +249,7 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
             d.off_out = np;
             for (int o = 0; o < u.n_out; ++o) a.ptrs[np++] = u.out[o];
         }
-        if (mode != zf::kModePlain) {
+        if (mode_uses_accum(mode)) {
             d.off_accum = np;
             for (int r = 0; r < n; ++r) a.ptrs[np++] = u.accum[r];
         }
@@ -599,4 +635,82 @@ ZERO_API int zero_selftest_wait_timeout(int64_t limit_ns, void* stream) {
     return cuda_status(zf::launch_wait_timeout_selftest(static_cast<uint64_t>(limit_ns),
                                                         static_cast<cudaStream_t>(stream)),
                        "self-test launch");
+}
+
+// ---------------------------------------------------- gradient clipping ----
+
+namespace {
+
+int clip_prepare(const zero_unit_t* units, int32_t n_units, int32_t micro_step, int32_t n_micro,
+                 std::vector<UnitView>& views) {
+    if (units == nullptr || n_units < 1) return fail(ZERO_ERR_INVALID_ARG, "no units");
+    if (n_units > 4096) return fail(ZERO_ERR_SIZE, "at most 4096 units per call");
+    views.resize(static_cast<size_t>(n_units));
+    for (int i = 0; i < n_units; ++i) {
+        const zero_unit_t& x = units[i];
+        views[i] = UnitView{x.layout, x.grads, x.master, x.m, x.v, x.accum, x.full_params, x.n_out};
+        if (x.accum == nullptr)
+            return fail(ZERO_ERR_INVALID_ARG, "clipping needs every unit's accum (gradient shards)");
+    }
+    if (n_micro < 1 || micro_step < 1 || micro_step > n_micro)
+        return fail(ZERO_ERR_INVALID_ARG, "need 1 <= micro_step <= n_micro");
+    return ZERO_OK;
+}
+
+}  // namespace
+
+ZERO_API int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t n_micro,
+                                       int64_t* bytes) {
+    if (bytes == nullptr) return fail(ZERO_ERR_INVALID_ARG, "bytes is NULL");
+    static thread_local std::vector<UnitView> views;
+    if (int rc = clip_prepare(units, n_units, n_micro, n_micro, views)) return rc;
+    for (const UnitView& u : views) {
+        if (int rc = check_layout(u.L)) return rc;
+    }
+    ClipPlan plan;
+    plan.dry_run = true;
+    const int mode = n_micro > 1 ? zf::kModeRsAvgNorm : zf::kModeRsNorm;
+    if (int rc = launch_units_staged(views.data(), n_units, mode, zf::AdamConsts{}, nullptr, &plan))
+        return rc;
+    *bytes = plan.slots_used * static_cast<int64_t>(sizeof(double));
+    return ok();
+}
+
+ZERO_API int zero_step_units_clip(const zero_unit_t* units, int32_t n_units, int32_t micro_step,
+                                  int32_t n_micro, const zero_adamw_t* hp, double max_norm,
+                                  void* workspace, int64_t workspace_bytes, float* norm_out,
+                                  void* stream) {
+    static thread_local std::vector<UnitView> views;
+    if (int rc = clip_prepare(units, n_units, micro_step, n_micro, views)) return rc;
+    const bool accumulating = n_micro > 1 && micro_step < n_micro;
+    for (const UnitView& u : views) {
+        if (int rc = check_unit(u, micro_step, n_micro, !accumulating)) return rc;
+        if (int rc = check_ptrs(const_cast<const float* const*>(u.accum), u.L->n_ranks, "accum"))
+            return rc;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (accumulating) {
+        return launch_units_staged(views.data(), n_units,
+                                   micro_step > 1 ? zf::kModeRsAdd : zf::kModeRsStore,
+                                   zf::AdamConsts{}, st);
+    }
+    if (int rc = check_hp(hp)) return rc;
+    if (!(max_norm > 0.0) || !std::isfinite(max_norm))
+        return fail(ZERO_ERR_INVALID_ARG, "max_norm must be a positive finite number");
+    if (workspace == nullptr) return fail(ZERO_ERR_INVALID_ARG, "workspace is NULL");
+    if (!aligned16(workspace)) return fail(ZERO_ERR_MISALIGNED, "workspace is not 16-byte aligned");
+    if (norm_out != nullptr && (reinterpret_cast<uintptr_t>(norm_out) & 3u) != 0)
+        return fail(ZERO_ERR_MISALIGNED, "norm_out is not 4-byte aligned");
+    ClipPlan plan;
+    plan.partials = static_cast<double*>(workspace);
+    plan.capacity = workspace_bytes / static_cast<int64_t>(sizeof(double));
+    plan.max_norm = max_norm;
+    plan.norm_out = norm_out;
+    const zf::AdamConsts k = derive_consts(hp, static_cast<double>(n_micro));
+    // Pass 1: averaged gradient into accum, per-CTA sums of its squares.
+    const int norm_mode = n_micro > 1 ? zf::kModeRsAvgNorm : zf::kModeRsNorm;
+    if (int rc = launch_units_staged(views.data(), n_units, norm_mode, k, st, &plan)) return rc;
+    // Pass 2: AdamW from the clipped averaged gradient, bf16 cast, all-gather.
+    plan.n_partials = static_cast<int32_t>(plan.slots_used);
+    return launch_units_staged(views.data(), n_units, zf::kModeFromShard, k, st, &plan);
 }

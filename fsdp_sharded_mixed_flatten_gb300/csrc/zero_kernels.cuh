@@ -94,13 +94,27 @@ struct MultiArgs {
     int32_t n_units;
     int32_t total_tiles;
     AdamConsts k;
+    // global gradient-norm clipping
+    double* partials;       // per-CTA sums of squares of the averaged gradient
+    int32_t partial_base;   // first slot a norm launch writes (one slot per CTA)
+    int32_t n_partials;     // slots an update launch reduces (fixed order)
+    double max_norm;        // clip threshold
+    float* norm_out;        // optional: total norm written by CTA 0 of an update launch
     UnitDesc unit[kMaxUnits];
     const void* ptrs[kMaxPtrs];
 };
 
 static_assert(sizeof(MultiArgs) <= 32764, "launch argument block limit");
 
-enum StepMode : int { kModePlain = 0, kModeAccumFinal = 1, kModeRsStore = 2, kModeRsAdd = 3 };
+enum StepMode : int {
+    kModePlain = 0,       // fused step from the gradients
+    kModeAccumFinal = 1,  // fused last micro-step: g = (accum + mean) / K
+    kModeRsStore = 2,     // reduce-scatter: accum = mean
+    kModeRsAdd = 3,       // reduce-scatter: accum += mean
+    kModeRsNorm = 4,      // clipping pass 1: accum = mean, per-CTA sum of mean^2
+    kModeRsAvgNorm = 5,   // clipping pass 1, last micro-step: accum = (accum + mean) / K, sum
+    kModeFromShard = 6    // clipping pass 2: AdamW from accum * clip coefficient
+};
 
 // Device-side status codes (g_zf_device_status); must match ZERO_DEVICE_*.
 constexpr int kDeviceOk = 0;
@@ -118,6 +132,9 @@ cudaError_t launch_all_gather(const ShardArgs<MAXR>& a, cudaStream_t stream);
 cudaError_t launch_flatten(const FlatArgs& a, int elem_bytes, int unflatten, cudaStream_t stream);
 // Bulk-copy staged fused step / reduce-scatter over the units of `a` (mode: StepMode).
 cudaError_t launch_staged_step(const MultiArgs& a, int mode, cudaStream_t stream);
+// Grid a staged launch of `mode` over `total_tiles` tiles uses (persistent:
+// at most one CTA per SM); norm launches write this many partial sums.
+int staged_grid(int mode, int total_tiles);
 // One CTA waiting on a barrier that nothing completes (tests the bounded wait).
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 // Read (and optionally clear) the device status word; synchronises `stream`.

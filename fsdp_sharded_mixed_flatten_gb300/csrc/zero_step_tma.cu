@@ -173,23 +173,28 @@ __device__ __forceinline__ const uint16_t* grad_ptr(const MultiArgs& a, const Un
     return ptr_at<const uint16_t*>(a, u->off_grads + k);
 }
 
+// Per mode: how many fp32 state arrays a tile's state block holds (master,
+// m, v, accumulator in that order; the reduce-scatter modes only the
+// accumulator), whether the gradients are read, and whether the mode writes
+// the averaged gradient to the accumulator (a reduce-scatter) or updates.
 template <int MODE>
-struct ModeTraits;
-// fused plain step: state = master, m, v
-template <> struct ModeTraits<kModePlain> { static constexpr int kStateArrays = 3; };
-// fused final micro-step: state = master, m, v, accumulator
-template <> struct ModeTraits<kModeAccumFinal> { static constexpr int kStateArrays = 4; };
-// reduce-scatter storing the mean: no state
-template <> struct ModeTraits<kModeRsStore> { static constexpr int kStateArrays = 0; };
-// reduce-scatter adding the mean to the accumulator: state = accumulator
-template <> struct ModeTraits<kModeRsAdd> { static constexpr int kStateArrays = 1; };
+struct ModeTraits {
+    static constexpr bool kReduceScatter =
+        MODE == kModeRsStore || MODE == kModeRsAdd || MODE == kModeRsNorm || MODE == kModeRsAvgNorm;
+    static constexpr bool kNorm = MODE == kModeRsNorm || MODE == kModeRsAvgNorm;
+    static constexpr bool kReadsGrads = MODE != kModeFromShard;
+    static constexpr int kStateArrays = MODE == kModePlain ? 3
+                                        : (MODE == kModeAccumFinal || MODE == kModeFromShard) ? 4
+                                        : (MODE == kModeRsAdd || MODE == kModeRsAvgNorm) ? 1
+                                                                                        : 0;
+};
 
 // State array `array` of rank r (order: master, m, v, accumulator; the
 // reduce-scatter modes only have the accumulator).
 template <int MODE>
 __device__ __forceinline__ float* state_ptr(const MultiArgs& a, const UnitDesc* u, int array,
                                             int r) {
-    if constexpr (MODE == kModeRsAdd || MODE == kModeRsStore) {
+    if constexpr (ModeTraits<MODE>::kReduceScatter) {
         return ptr_at<float*>(a, u->off_accum + r);
     } else {
         const int off = array == 0 ? u->off_master
@@ -242,7 +247,8 @@ __device__ void producer_loop(const MultiArgs& a, uint8_t* smem, uint64_t* full,
             ++it;
         }
         const uint32_t gbytes = static_cast<uint32_t>(g.a1 - g.a0) * 2;
-        const int groups = (n_ranks + kRanksPerStage - 1) / kRanksPerStage;
+        const int groups =
+            ModeTraits<MODE>::kReadsGrads ? (n_ranks + kRanksPerStage - 1) / kRanksPerStage : 0;
         bool stop = false;
         for (int grp = 0; grp < groups; ++grp) {
             const uint32_t slot = it % kStages, parity = ((it / kStages) & 1) ^ 1;
@@ -271,12 +277,13 @@ __device__ void producer_loop(const MultiArgs& a, uint8_t* smem, uint64_t* full,
 template <int MODE>
 __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t* full,
                               uint64_t* empty, volatile int* abort_flag,
-                              unsigned int* consumed_min) {
+                              unsigned int* consumed_min, float clip_coef, double* warp_sq) {
     constexpr int NS = ModeTraits<MODE>::kStateArrays;
     const int tid = threadIdx.x;  // 0..kConsumers-1
     const int lane = tid & 31;
     uint32_t it = 0;
     bool ok = true;
+    float sq_s = 0.0f, sq_c = 0.0f;   // compensated sum of squares (norm modes)
     for (int tile = blockIdx.x; tile < a.total_tiles && ok; tile += gridDim.x) {
         const TileGeom g = tile_geom(a, tile);
         const UnitDesc* u = g.u;
@@ -320,7 +327,8 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
             c[q] = make_float2(0.0f, 0.0f);
         }
         const bool vec = (nv == kVec) && (e + kVec <= g.a1);
-        const int groups = (n_ranks + kRanksPerStage - 1) / kRanksPerStage;
+        const int groups =
+            ModeTraits<MODE>::kReadsGrads ? (n_ranks + kRanksPerStage - 1) / kRanksPerStage : 0;
         for (int grp = 0; grp < groups; ++grp) {
             const uint32_t slot = it % kStages, parity = (it / kStages) & 1;
             if (!mbar_wait_bounded(smem_u32(&full[slot]), parity, abort_flag, kWaitLimitNs)) {
@@ -368,12 +376,18 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
             mean[2 * q + 1] = finish_mean(s[q].y, c[q].y, u->n_ranks_f, u->inv_n, u->n_pow2);
         }
 
-        if constexpr (MODE == kModeRsStore || MODE == kModeRsAdd) {
+        if constexpr (ModeTraits<MODE>::kReduceScatter) {
             float out[8];
 #pragma unroll
             for (int t = 0; t < kVec; ++t) {
                 out[t] = mean[t];
                 if constexpr (MODE == kModeRsAdd) out[t] = __fadd_rn(st[0][t], mean[t]);
+                if constexpr (MODE == kModeRsAvgNorm) {
+                    out[t] = __fdiv_rn(__fadd_rn(st[0][t], mean[t]), a.k.divisor);
+                }
+                if constexpr (ModeTraits<MODE>::kNorm) {
+                    if (t < nv) two_sum_add1(sq_s, sq_c, __fmul_rn(out[t], out[t]));
+                }
             }
             float* dst = state_ptr<MODE>(a, u, 0, g.r) + j;
             if (nv == kVec) {
@@ -387,6 +401,9 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
                 float gr = mean[t];
                 if constexpr (MODE == kModeAccumFinal) {
                     gr = __fdiv_rn(__fadd_rn(st[3][t], mean[t]), a.k.divisor);
+                }
+                if constexpr (MODE == kModeFromShard) {
+                    gr = clip_coef == 1.0f ? st[3][t] : __fmul_rn(st[3][t], clip_coef);
                 }
                 adamw_update(a.k, gr, st[0][t], st[1][t], st[2][t]);
             }
@@ -419,6 +436,13 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
         }
     }
     if (lane == 0) atomicMin(consumed_min, it);
+    if constexpr (ModeTraits<MODE>::kNorm) {
+        // Warp sum of the threads' compensated sums, in double, fixed order.
+        double w = static_cast<double>(sq_s) + static_cast<double>(sq_c);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) w += __shfl_down_sync(0xFFFFFFFFu, w, off);
+        if (lane == 0) warp_sq[tid >> 5] = w;
+    }
 }
 
 }  // namespace
@@ -432,6 +456,8 @@ staged_step_kernel(const __grid_constant__ MultiArgs a) {
     __shared__ int abort_flag;
     __shared__ uint32_t issued;
     __shared__ unsigned int consumed_min;
+    __shared__ float clip_coef;
+    __shared__ double warp_sq[kConsumerWarps];
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
@@ -440,6 +466,17 @@ staged_step_kernel(const __grid_constant__ MultiArgs a) {
         abort_flag = 0;
         issued = 0;
         consumed_min = 0xFFFFFFFFu;
+        clip_coef = 1.0f;
+        if constexpr (MODE == kModeFromShard) {
+            // Total norm from the norm launches' partial sums, in a fixed order,
+            // so every CTA derives the same coefficient.
+            double total = 0.0;
+            for (int i = 0; i < a.n_partials; ++i) total += a.partials[i];
+            const double norm = sqrt(total);
+            const double coef = a.max_norm / (norm + 1e-6);
+            clip_coef = coef >= 1.0 ? 1.0f : static_cast<float>(coef);
+            if (blockIdx.x == 0 && a.norm_out != nullptr) *a.norm_out = static_cast<float>(norm);
+        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -447,9 +484,16 @@ staged_step_kernel(const __grid_constant__ MultiArgs a) {
     if (threadIdx.x >= kConsumers) {
         if (threadIdx.x == kConsumers) producer_loop<MODE>(a, smem, full, empty, &abort_flag, &issued);
     } else {
-        consumer_loop<MODE>(a, smem, full, empty, &abort_flag, &consumed_min);
+        consumer_loop<MODE>(a, smem, full, empty, &abort_flag, &consumed_min, clip_coef, warp_sq);
     }
     __syncthreads();
+    if constexpr (ModeTraits<MODE>::kNorm) {
+        if (threadIdx.x == 0) {
+            double total = 0.0;
+            for (int w = 0; w < kConsumerWarps; ++w) total += warp_sq[w];
+            a.partials[a.partial_base + blockIdx.x] = total;
+        }
+    }
     if (threadIdx.x == 0 && abort_flag) {
         // Let every copy this CTA issued land before shared memory goes away.
         for (uint32_t it = consumed_min; it < issued; ++it) {
@@ -460,16 +504,37 @@ staged_step_kernel(const __grid_constant__ MultiArgs a) {
     }
 }
 
+constexpr size_t kStagedSmem = static_cast<size_t>(kStages) * kStageBytes;
+
+template <int MODE>
+static int grid_for(int total_tiles) {
+    const void* kfn = reinterpret_cast<const void*>(&staged_step_kernel<MODE>);
+    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                         static_cast<int>(kStagedSmem));
+    return persistent_grid(kfn, kTmaThreads, kStagedSmem, total_tiles);
+}
+
 template <int MODE>
 static cudaError_t launch_staged(const MultiArgs& a, cudaStream_t stream) {
     const void* kfn = reinterpret_cast<const void*>(&staged_step_kernel<MODE>);
-    const size_t smem = static_cast<size_t>(kStages) * kStageBytes;
     cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
+                                         static_cast<int>(kStagedSmem));
     if (e != cudaSuccess) return e;
-    const int grid = persistent_grid(kfn, kTmaThreads, smem, a.total_tiles);
-    staged_step_kernel<MODE><<<grid, kTmaThreads, smem, stream>>>(a);
+    const int grid = persistent_grid(kfn, kTmaThreads, kStagedSmem, a.total_tiles);
+    staged_step_kernel<MODE><<<grid, kTmaThreads, kStagedSmem, stream>>>(a);
     return cudaGetLastError();
+}
+
+int staged_grid(int mode, int total_tiles) {
+    switch (mode) {
+        case kModePlain: return grid_for<kModePlain>(total_tiles);
+        case kModeAccumFinal: return grid_for<kModeAccumFinal>(total_tiles);
+        case kModeRsStore: return grid_for<kModeRsStore>(total_tiles);
+        case kModeRsAdd: return grid_for<kModeRsAdd>(total_tiles);
+        case kModeRsNorm: return grid_for<kModeRsNorm>(total_tiles);
+        case kModeRsAvgNorm: return grid_for<kModeRsAvgNorm>(total_tiles);
+        default: return grid_for<kModeFromShard>(total_tiles);
+    }
 }
 
 cudaError_t launch_staged_step(const MultiArgs& a, int mode, cudaStream_t stream) {
@@ -478,7 +543,10 @@ cudaError_t launch_staged_step(const MultiArgs& a, int mode, cudaStream_t stream
         case kModePlain: return launch_staged<kModePlain>(a, stream);
         case kModeAccumFinal: return launch_staged<kModeAccumFinal>(a, stream);
         case kModeRsStore: return launch_staged<kModeRsStore>(a, stream);
-        default: return launch_staged<kModeRsAdd>(a, stream);
+        case kModeRsAdd: return launch_staged<kModeRsAdd>(a, stream);
+        case kModeRsNorm: return launch_staged<kModeRsNorm>(a, stream);
+        case kModeRsAvgNorm: return launch_staged<kModeRsAvgNorm>(a, stream);
+        default: return launch_staged<kModeFromShard>(a, stream);
     }
 }
 

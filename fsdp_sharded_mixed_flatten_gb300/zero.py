@@ -94,6 +94,12 @@ def load() -> ctypes.CDLL:
             fn.restype = ctypes.c_int
         lib.zero_step_units.argtypes = [ctypes.POINTER(ZeroUnit), i32, i32, i32, hp, p]
         lib.zero_step_units.restype = ctypes.c_int
+        lib.zero_clip_workspace_bytes.argtypes = [ctypes.POINTER(ZeroUnit), i32, i32,
+                                                  ctypes.POINTER(ctypes.c_int64)]
+        lib.zero_clip_workspace_bytes.restype = ctypes.c_int
+        lib.zero_step_units_clip.argtypes = [ctypes.POINTER(ZeroUnit), i32, i32, i32, hp,
+                                             ctypes.c_double, p, i64, p, p]
+        lib.zero_step_units_clip.restype = ctypes.c_int
         lib.zero_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_int32), i32]
         lib.zero_device_status.restype = ctypes.c_int
         lib.zero_selftest_wait_timeout.argtypes = [i64, p]
@@ -256,8 +262,9 @@ def zero_selftest_wait_timeout(limit_ns: int, stream=None):
            "zero_selftest_wait_timeout")
 
 
-def zero_step_units(units, micro_step: int, n_micro: int, hp, stream=None):
-    """units: sequence of (grads, master, m, v, accum or None, full_params, layout)."""
+def _unit_array(units):
+    """Marshal (grads, master, m, v, accum or None, full_params, layout) tuples
+    into a zero_unit_t array; returns (array, keep-alive list)."""
     n = len(units)
     arr = (ZeroUnit * max(n, 1))()
     keep = []
@@ -271,7 +278,35 @@ def zero_step_units(units, micro_step: int, n_micro: int, hp, stream=None):
         arr[i].accum = ctypes.cast(tabs[4], ctypes.c_void_p) if tabs[4] is not None else None
         arr[i].full_params = ctypes.cast(tabs[5], ctypes.c_void_p)
         arr[i].n_out = len(full)
+    return arr, keep
+
+
+def zero_step_units(units, micro_step: int, n_micro: int, hp, stream=None):
+    """units: sequence of (grads, master, m, v, accum or None, full_params, layout)."""
+    arr, keep = _unit_array(units)
     h = _hp(hp)
-    _check(load().zero_step_units(arr, n, int(micro_step), int(n_micro),
+    _check(load().zero_step_units(arr, len(units), int(micro_step), int(n_micro),
                                   ctypes.byref(h) if h is not None else None, _stream(stream)),
            "zero_step_units")
+
+
+def zero_clip_workspace_bytes(units, n_micro: int = 1) -> int:
+    arr, keep = _unit_array(units)
+    out = ctypes.c_int64(0)
+    _check(load().zero_clip_workspace_bytes(arr, len(units), int(n_micro), ctypes.byref(out)),
+           "zero_clip_workspace_bytes")
+    return int(out.value)
+
+
+def zero_step_units_clip(units, micro_step: int, n_micro: int, hp, max_norm: float, workspace,
+                         workspace_bytes: int, norm_out=None, stream=None):
+    """zero_step_units with global gradient-norm clipping; every unit needs an
+    accumulator (it receives the averaged gradient).  workspace: device
+    buffer of at least zero_clip_workspace_bytes(units, n_micro) bytes."""
+    arr, keep = _unit_array(units)
+    h = _hp(hp)
+    _check(load().zero_step_units_clip(arr, len(units), int(micro_step), int(n_micro),
+                                       ctypes.byref(h) if h is not None else None,
+                                       float(max_norm), _addr(workspace) or None,
+                                       int(workspace_bytes), _addr(norm_out) or None,
+                                       _stream(stream)), "zero_step_units_clip")

@@ -259,6 +259,40 @@ typedef struct zero_unit {
 int zero_step_units(const zero_unit_t* units, int32_t n_units, int32_t micro_step,
                     int32_t n_micro, const zero_adamw_t* hp, void* stream);
 
+/*
+ * zero_step_units_clip -- device.  zero_step_units with global gradient-norm
+ * clipping ([DZ] section 6: a norm over the whole model needs a reduction
+ * across every shard).  Reading: the clip-by-total-L2-norm rule -- over every
+ * element of every unit's averaged gradient g (the reduce-scatter mean, or at
+ * the last micro-step the accumulated mean / n_micro),
+ *   norm = sqrt(sum g^2),  coef = max_norm / (norm + 1e-6),
+ *   g <- g * coef (fp32) when coef < 1,
+ * then AdamW, bf16 cast and all-gather as in zero_step.
+ *   Every unit needs `accum` (fp32, [n_ranks] x S): it receives the averaged,
+ *   unclipped gradient of this step (at accumulation micro-steps it is the
+ *   usual accumulator, and the call is the same as zero_step_units).
+ *   workspace        caller-owned device scratch of at least the size
+ *                    zero_clip_workspace_bytes reports, 16-byte aligned; it
+ *                    holds per-CTA partial sums between the two passes
+ *   norm_out         NULL, or a device float receiving the total norm
+ * Two passes over HBM: the first reads the gradients and writes the averaged
+ * gradient (2*N_d + 4 bytes per element, +4 at a last micro-step), the second
+ * reads it with the state and writes state and parameters (30 bytes).
+ * Deterministic: the partial sums are reduced in a fixed order.
+ * Errors: as zero_step_units; ZERO_ERR_SIZE if the workspace is too small.
+ */
+int zero_step_units_clip(const zero_unit_t* units, int32_t n_units, int32_t micro_step,
+                         int32_t n_micro, const zero_adamw_t* hp, double max_norm,
+                         void* workspace, int64_t workspace_bytes, float* norm_out, void* stream);
+
+/*
+ * zero_clip_workspace_bytes -- host.  Workspace size zero_step_units_clip
+ * needs for these units on the current device (one double per CTA of each
+ * norm launch).
+ */
+int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t n_micro,
+                              int64_t* bytes);
+
 /* Message for the last non-OK return on the calling thread ("" if none). */
 const char* zero_last_error(void);
 
