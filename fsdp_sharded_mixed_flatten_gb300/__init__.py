@@ -10,7 +10,7 @@ from .zero import (ZERO_MAX_RANKS, ZeroAdamW, ZeroError, ZeroLayout, load, zero_
                    zero_adamw_shard_step, zero_all_gather, zero_device_status, zero_flat_layout,
                    zero_flatten, zero_last_error, zero_reduce_scatter, zero_selftest_wait_timeout,
                    zero_shard_segments, zero_step, zero_step_units, zero_step_units_clip,
-                   zero_clip_workspace_bytes, zero_unflatten)
+                   zero_step_units_clip_noalloc, zero_clip_workspace_bytes, zero_unflatten)
 
 __all__ = [
     "ZERO_MAX_RANKS", "ZeroAdamW", "ZeroError", "ZeroLayout", "load", "zero_abi_version",
@@ -18,6 +18,6 @@ __all__ = [
     "zero_flatten",
     "zero_last_error", "zero_reduce_scatter", "zero_selftest_wait_timeout",
     "zero_shard_segments", "zero_step", "zero_step_units", "zero_step_units_clip",
-    "zero_clip_workspace_bytes",
+    "zero_clip_workspace_bytes", "zero_step_units_clip_noalloc",
     "zero_unflatten",
 ]

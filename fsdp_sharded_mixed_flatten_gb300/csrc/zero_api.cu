@@ -9,6 +9,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <limits>
+#include <mutex>
 #include <vector>
 
 #include "zero_flat.h"
@@ -713,4 +714,104 @@ ZERO_API int zero_step_units_clip(const zero_unit_t* units, int32_t n_units, int
     // Pass 2: AdamW from the clipped averaged gradient, bf16 cast, all-gather.
     plan.n_partials = static_cast<int32_t>(plan.slots_used);
     return launch_units_staged(views.data(), n_units, zf::kModeFromShard, k, st, &plan);
+}
+
+// ------------------------------------------------ no-allocation variant ----
+//
+// zero_step_units_clip needs a small device workspace between its two passes.
+// Some callers cannot allocate device memory for it: a runtime that hands all
+// device memory to its own pool at start-up and lets no library allocate on
+// the side, or a deployment whose device-memory budget is fixed before the
+// optimizer runs.  zero_step_units_clip_noalloc keeps the partial sums in the
+// array below instead, which the module reserves when it is loaded (every GPU
+// that loads this library holds it, 32 KB, until the process exits).
+
+static __device__ __align__(256) double g_noalloc_clip_partials[ZERO_NOALLOC_CLIP_SLOTS];
+
+namespace {
+
+constexpr int kNoAllocMaxDevices = 64;
+constexpr int kNoAllocMaxUnits = 256;
+
+// Device address of the scratch array for the current device.  Host code may
+// not use the array's name as a device address (it is a host-side stand-in),
+// so the address is looked up once per device with that device current.
+int noalloc_scratch(double** out) {
+    int dev = -1;
+    if (int rc = cuda_status(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
+    if (dev < 0 || dev >= kNoAllocMaxDevices)
+        return fail(ZERO_ERR_SIZE, "device index %d beyond %d", dev, kNoAllocMaxDevices);
+    static std::mutex mu;
+    static double* ptrs[kNoAllocMaxDevices] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (ptrs[dev] == nullptr) {
+        void* p = nullptr;
+        if (int rc = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_clip_partials),
+                                 "cudaGetSymbolAddress(clipping scratch)"))
+            return rc;
+        ptrs[dev] = static_cast<double*>(p);
+    }
+    *out = ptrs[dev];
+    return ZERO_OK;
+}
+
+}  // namespace
+
+ZERO_API int zero_step_units_clip_noalloc(const zero_unit_t* units, int32_t n_units,
+                                          int32_t micro_step, int32_t n_micro,
+                                          const zero_adamw_t* hp, double max_norm,
+                                          float* norm_out, void* stream) {
+    if (units == nullptr || n_units < 1) return fail(ZERO_ERR_INVALID_ARG, "no units");
+    if (n_units > kNoAllocMaxUnits)
+        return fail(ZERO_ERR_SIZE, "at most %d units per call without a workspace",
+                    kNoAllocMaxUnits);
+    if (n_micro < 1 || micro_step < 1 || micro_step > n_micro)
+        return fail(ZERO_ERR_INVALID_ARG, "need 1 <= micro_step <= n_micro");
+    UnitView views[kNoAllocMaxUnits];
+    const bool accumulating = n_micro > 1 && micro_step < n_micro;
+    for (int i = 0; i < n_units; ++i) {
+        const zero_unit_t& x = units[i];
+        views[i] = UnitView{x.layout, x.grads, x.master, x.m, x.v, x.accum, x.full_params, x.n_out};
+        if (x.accum == nullptr)
+            return fail(ZERO_ERR_INVALID_ARG, "clipping needs every unit's accum (gradient shards)");
+        if (int rc = check_unit(views[i], micro_step, n_micro, !accumulating)) return rc;
+        if (int rc = check_ptrs(const_cast<const float* const*>(x.accum), x.layout->n_ranks,
+                                "accum"))
+            return rc;
+    }
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (accumulating) {
+        return launch_units_staged(views, n_units,
+                                   micro_step > 1 ? zf::kModeRsAdd : zf::kModeRsStore,
+                                   zf::AdamConsts{}, st);
+    }
+    if (int rc = check_hp(hp)) return rc;
+    if (!(max_norm > 0.0) || !std::isfinite(max_norm))
+        return fail(ZERO_ERR_INVALID_ARG, "max_norm must be a positive finite number");
+    if (norm_out != nullptr && (reinterpret_cast<uintptr_t>(norm_out) & 3u) != 0)
+        return fail(ZERO_ERR_MISALIGNED, "norm_out is not 4-byte aligned");
+    const int norm_mode = n_micro > 1 ? zf::kModeRsAvgNorm : zf::kModeRsNorm;
+    // Count the partial-sum slots first, so that an oversized call launches nothing.
+    ClipPlan count;
+    count.dry_run = true;
+    if (int rc = launch_units_staged(views, n_units, norm_mode, zf::AdamConsts{}, st, &count))
+        return rc;
+    if (count.slots_used > ZERO_NOALLOC_CLIP_SLOTS)
+        return fail(ZERO_ERR_SIZE,
+                    "these units need %lld partial-sum slots; the built-in scratch holds %d "
+                    "(use zero_step_units_clip with a workspace)",
+                    (long long)count.slots_used, ZERO_NOALLOC_CLIP_SLOTS);
+    double* scratch = nullptr;
+    if (int rc = noalloc_scratch(&scratch)) return rc;
+    ClipPlan plan;
+    plan.partials = scratch;
+    plan.capacity = ZERO_NOALLOC_CLIP_SLOTS;
+    plan.max_norm = max_norm;
+    plan.norm_out = norm_out;
+    const zf::AdamConsts k = derive_consts(hp, static_cast<double>(n_micro));
+    // Every partial slot the update pass reads is written by this call's norm
+    // pass first, so the scratch needs no clearing.
+    if (int rc = launch_units_staged(views, n_units, norm_mode, k, st, &plan)) return rc;
+    plan.n_partials = static_cast<int32_t>(plan.slots_used);
+    return launch_units_staged(views, n_units, zf::kModeFromShard, k, st, &plan);
 }

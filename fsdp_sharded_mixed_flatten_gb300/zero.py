@@ -100,6 +100,9 @@ def load() -> ctypes.CDLL:
         lib.zero_step_units_clip.argtypes = [ctypes.POINTER(ZeroUnit), i32, i32, i32, hp,
                                              ctypes.c_double, p, i64, p, p]
         lib.zero_step_units_clip.restype = ctypes.c_int
+        lib.zero_step_units_clip_noalloc.argtypes = [ctypes.POINTER(ZeroUnit), i32, i32, i32,
+                                                     hp, ctypes.c_double, p, p]
+        lib.zero_step_units_clip_noalloc.restype = ctypes.c_int
         lib.zero_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_int32), i32]
         lib.zero_device_status.restype = ctypes.c_int
         lib.zero_selftest_wait_timeout.argtypes = [i64, p]
@@ -310,3 +313,20 @@ def zero_step_units_clip(units, micro_step: int, n_micro: int, hp, max_norm: flo
                                        float(max_norm), _addr(workspace) or None,
                                        int(workspace_bytes), _addr(norm_out) or None,
                                        _stream(stream)), "zero_step_units_clip")
+
+
+ZERO_NOALLOC_CLIP_SLOTS = 4096
+
+
+def zero_step_units_clip_noalloc(units, micro_step: int, n_micro: int, hp, max_norm: float,
+                                 norm_out=None, stream=None):
+    """zero_step_units_clip without a caller workspace, for callers that cannot
+    allocate device memory: the partial sums live in a fixed 32 KB scratch
+    array inside the library, shared by every call (serialise calls that could
+    overlap on the GPU)."""
+    arr, keep = _unit_array(units)
+    h = _hp(hp)
+    _check(load().zero_step_units_clip_noalloc(arr, len(units), int(micro_step), int(n_micro),
+                                               ctypes.byref(h) if h is not None else None,
+                                               float(max_norm), _addr(norm_out) or None,
+                                               _stream(stream)), "zero_step_units_clip_noalloc")

@@ -293,6 +293,33 @@ int zero_step_units_clip(const zero_unit_t* units, int32_t n_units, int32_t micr
 int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t n_micro,
                               int64_t* bytes);
 
+/*
+ * zero_step_units_clip_noalloc -- device.  The same computation as
+ * zero_step_units_clip for callers that cannot allocate device memory for the
+ * workspace: a runtime that gives all device memory to its own pool at
+ * start-up and allows no allocation on the side, or a deployment whose device
+ * memory budget is fixed before the optimizer runs.  This call allocates
+ * nothing (no cudaMalloc, cudaFree or allocating library routine); the partial
+ * sums live in a scratch array of ZERO_NOALLOC_CLIP_SLOTS doubles (32 KB) that
+ * the library reserves on every GPU that loads it, until the process exits.
+ * No counterpart on the pages: this is a deployment variant only.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before any
+ *     stream capture.
+ *   - Every call shares the one array.  Each call writes every slot it later
+ *     reads, so nothing needs clearing, but calls that overlap on the GPU
+ *     (two streams at once) race on it: serialise them.
+ *   - At most 256 units per call, and the units may need at most
+ *     ZERO_NOALLOC_CLIP_SLOTS partial sums (one per CTA of each norm launch);
+ *     larger calls are rejected with ZERO_ERR_SIZE before anything is
+ *     launched -- use zero_step_units_clip with a workspace then.
+ * Arguments and results otherwise as zero_step_units_clip.
+ */
+#define ZERO_NOALLOC_CLIP_SLOTS 4096
+int zero_step_units_clip_noalloc(const zero_unit_t* units, int32_t n_units, int32_t micro_step,
+                                 int32_t n_micro, const zero_adamw_t* hp, double max_norm,
+                                 float* norm_out, void* stream);
+
 /* Message for the last non-OK return on the calling thread ("" if none). */
 const char* zero_last_error(void);
 
