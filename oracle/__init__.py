@@ -70,6 +70,10 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_adamw.restype = None
     lib.oracle_all_gather.argtypes = [p, i32, i64, p]
     lib.oracle_all_gather.restype = None
+    lib.oracle_zero1_accumulate.argtypes = [p, p, i32, i64, i32]
+    lib.oracle_zero1_accumulate.restype = None
+    lib.oracle_zero1_step.argtypes = [p, i32, i64, i32, p, p, p, p, f64, f64, f64, f64, f64, i64]
+    lib.oracle_zero1_step.restype = ctypes.c_int
     lib.oracle_sum_squares.argtypes = [p, i64]
     lib.oracle_sum_squares.restype = f64
     lib.oracle_clip_coefficient.argtypes = [f64, f64]
@@ -199,6 +203,32 @@ class Oracle:
             _f32(a)
         self.lib.oracle_adamw(_ptr(theta), _ptr(m), _ptr(v), _ptr(np.ascontiguousarray(g)),
                               theta.size, lr, beta1, beta2, eps, weight_decay, int(step))
+
+    # -- ZeRO-1 local accumulation ---------------------------------------
+    def zero1_accumulate(self, grads, acc_full, first: bool) -> None:
+        """grads: (n_ranks, P_pad) uint16; acc_full: (n_ranks, P_pad) float32, in place."""
+        grads = _u16(grads)
+        n_ranks, P_pad = grads.shape
+        if acc_full.shape != grads.shape or acc_full.dtype != np.float32 or \
+                not acc_full.flags["C_CONTIGUOUS"]:
+            raise ValueError("acc_full must be C-contiguous float32 (n_ranks, P_pad)")
+        self.lib.oracle_zero1_accumulate(_ptr(grads), _ptr(acc_full), n_ranks, P_pad,
+                                         int(bool(first)))
+
+    def zero1_step(self, acc_full, master, m, v, *, n_micro, lr, beta1, beta2, eps,
+                   weight_decay, step):
+        """acc_full: (n_ranks, P_pad) float32; master/m/v: (n_ranks, S) float32,
+        updated in place.  Returns the (P_pad,) uint16 gathered parameters."""
+        acc_full = _f32(acc_full)
+        n_ranks, P_pad = acc_full.shape
+        S = P_pad // n_ranks
+        full = np.empty(P_pad, dtype=np.uint16)
+        rc = self.lib.oracle_zero1_step(_ptr(acc_full), n_ranks, S, int(n_micro), _ptr(master),
+                                        _ptr(m), _ptr(v), _ptr(full), lr, beta1, beta2, eps,
+                                        weight_decay, int(step))
+        if rc != 0:
+            raise ValueError("bad arguments to oracle_zero1_step")
+        return full
 
     # -- gradient clipping ----------------------------------------------
     def sum_squares(self, g) -> float:

@@ -230,6 +230,73 @@ void oracle_adamw(float* theta, float* m, float* v, const float* g, int64_t n, d
     }
 }
 
+/* ------------------------------------- ZeRO-1 local accumulation --------- */
+
+/*
+ * ZeRO-1 gradient accumulation ([L5] section 3, on gradient accumulation:
+ * with ZeRO-1 each rank still holds the full gradient, so it can accumulate
+ * the micro-batches locally and reduce-scatter only once, at the last one;
+ * section 2 note: the fp32 accumulator then costs the full +4 Psi per rank).
+ * acc_full: n_ranks rows of P_pad fp32 (each rank's own full accumulator);
+ * acc = (first ? 0 : acc) + widen(grad), rounded once to fp32.
+ */
+void oracle_zero1_accumulate(const uint16_t* grads, float* acc_full, int32_t n_ranks, int64_t P_pad,
+                             int32_t first)
+{
+    for (int32_t k = 0; k < n_ranks; ++k) {
+        for (int64_t e = 0; e < P_pad; ++e) {
+            int64_t idx = (int64_t)k * P_pad + e;
+            double g = (double)oracle_bf16_to_f32(grads[idx]);
+            double prev = first ? 0.0 : (double)acc_full[idx];
+            acc_full[idx] = (float)(prev + g);
+        }
+    }
+}
+
+/*
+ * ZeRO-1 optimizer step after n_micro accumulated micro-batches: the one
+ * reduce-scatter averages the ranks' fp32 accumulators (sum in double, one
+ * rounding), the result is divided by n_micro (one rounding), then every rank
+ * runs AdamW on its shard, rounds to bf16, and the shards are all-gathered.
+ */
+int oracle_zero1_step(const float* acc_full, int32_t n_ranks, int64_t S, int32_t n_micro,
+                      float* master, float* m, float* v, uint16_t* full_out, double lr,
+                      double beta1, double beta2, double eps, double weight_decay, int64_t step)
+{
+    if (n_ranks < 1 || S < 1 || n_micro < 1 || step < 1) {
+        return -1;
+    }
+    int64_t P_pad = (int64_t)n_ranks * S;
+    float* g = (float*)malloc((size_t)P_pad * sizeof(float));
+    uint16_t* p_shards = (uint16_t*)malloc((size_t)P_pad * sizeof(uint16_t));
+    if (g == NULL || p_shards == NULL) {
+        free(g);
+        free(p_shards);
+        return -1;
+    }
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        for (int64_t i = 0; i < S; ++i) {
+            int64_t e = (int64_t)r * S + i;
+            double sum = 0.0;
+            for (int32_t k = 0; k < n_ranks; ++k) {
+                sum = sum + (double)acc_full[(int64_t)k * P_pad + e];
+            }
+            float mean = (float)(sum / (double)n_ranks);
+            g[e] = (float)((double)mean / (double)n_micro);
+        }
+    }
+    for (int32_t r = 0; r < n_ranks; ++r) {
+        int64_t off = (int64_t)r * S;
+        oracle_adamw(master + off, m + off, v + off, g + off, S, lr, beta1, beta2, eps,
+                     weight_decay, step);
+        oracle_round_to_bf16(master + off, S, p_shards + off);
+    }
+    oracle_all_gather(p_shards, n_ranks, S, full_out);
+    free(g);
+    free(p_shards);
+    return 0;
+}
+
 /* ------------------------------------------------ gradient clipping ------- */
 
 /*

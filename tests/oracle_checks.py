@@ -486,6 +486,45 @@ def check_clipped_units_step_vs_torch(o):
         assert np.all(np.abs(u["master"][0] - ref) <= 2.0 ** -20 * (np.abs(ref) + HP["lr"]))
 
 
+def check_zero1_accumulation(o):
+    """ZeRO-1 (accumulate full gradients locally, one reduce-scatter at the end):
+    with one micro-step it is the plain step; with K equal micro-batches
+    (power-of-two K, exact sums) it is the plain step; with exactly
+    representable gradients it equals the ZeRO-2 path (reduce-scatter every
+    micro-step), because both reach the exact mean."""
+    rng = np.random.default_rng(14)
+    n_ranks, P = 4, 58
+    grads, theta, S = _random_state(rng, n_ranks, P)
+    base = theta.reshape(n_ranks, S)
+    P_pad = n_ranks * S
+    for K in (1, 2, 4):
+        acc = np.full((n_ranks, P_pad), 7.0, np.float32)   # garbage: first micro-step resets
+        for k in range(1, K + 1):
+            o.zero1_accumulate(grads, acc, first=(k == 1))
+        ma, m1, v1 = base.copy(), np.zeros_like(base), np.zeros_like(base)
+        full = o.zero1_step(acc, ma, m1, v1, n_micro=K, step=1, **HP)
+        mb, m2, v2 = base.copy(), np.zeros_like(base), np.zeros_like(base)
+        full_plain = o.zero_step(grads, mb, m2, v2, step=1, **HP)
+        assert np.array_equal(full, full_plain)
+        assert np.array_equal(ma.view(np.uint32), mb.view(np.uint32))
+        assert np.array_equal(m1.view(np.uint32), m2.view(np.uint32))
+    mk = [torch_bf16_bits((rng.integers(-32, 32, size=(n_ranks, P_pad)) / 1024.0)
+                          .astype(np.float32)) for _ in range(4)]
+    acc = np.zeros((n_ranks, P_pad), np.float32)
+    for k, g in enumerate(mk, start=1):
+        o.zero1_accumulate(g, acc, first=(k == 1))
+    # each rank's accumulator is the exact sum of its own micro-batches
+    assert np.array_equal(acc, np.sum([bits_to_f32(g) for g in mk], axis=0).astype(np.float32))
+    ma, m1, v1 = base.copy(), np.zeros_like(base), np.zeros_like(base)
+    full1 = o.zero1_step(acc, ma, m1, v1, n_micro=4, step=1, **HP)
+    mb, m2, v2 = base.copy(), np.zeros_like(base), np.zeros_like(base)
+    acc2 = np.zeros_like(base)
+    for k, g in enumerate(mk, start=1):
+        full2 = o.zero_step(g, mb, m2, v2, step=1, accum=acc2, micro_step=k, n_micro=4, **HP)
+    assert np.array_equal(full1, full2)
+    assert np.array_equal(ma.view(np.uint32), mb.view(np.uint32))
+
+
 ALL_CHECKS = [
     check_bf16_rounding,
     check_bf16_widening,
@@ -505,4 +544,5 @@ ALL_CHECKS = [
     check_clip_coefficient_vs_torch,
     check_clip_closed_forms,
     check_clipped_units_step_vs_torch,
+    check_zero1_accumulation,
 ]
