@@ -70,6 +70,8 @@ def _declare(lib: ctypes.CDLL) -> ctypes.CDLL:
     lib.oracle_adamw.restype = None
     lib.oracle_all_gather.argtypes = [p, i32, i64, p]
     lib.oracle_all_gather.restype = None
+    lib.oracle_param_shard_bounds.argtypes = [i64, i64, i32, i32, p, p]
+    lib.oracle_param_shard_bounds.restype = None
     lib.oracle_zero1_accumulate.argtypes = [p, p, i32, i64, i32]
     lib.oracle_zero1_accumulate.restype = None
     lib.oracle_zero1_step.argtypes = [p, i32, i64, i32, p, p, p, p, f64, f64, f64, f64, f64, i64]
@@ -203,6 +205,40 @@ class Oracle:
             _f32(a)
         self.lib.oracle_adamw(_ptr(theta), _ptr(m), _ptr(v), _ptr(np.ascontiguousarray(g)),
                               theta.size, lr, beta1, beta2, eps, weight_decay, int(step))
+
+    # -- FSDP2 per-parameter Shard(0) -----------------------------------
+    def param_shard_bounds(self, dim0: int, row_numel: int, n_ranks: int, rank: int):
+        b, e = ctypes.c_int64(0), ctypes.c_int64(0)
+        self.lib.oracle_param_shard_bounds(int(dim0), int(row_numel), int(n_ranks), int(rank),
+                                           ctypes.byref(b), ctypes.byref(e))
+        return int(b.value), int(e.value)
+
+    def param_sharded_step(self, params, *, lr, beta1, beta2, eps, weight_decay, step):
+        """One step over per-parameter Shard(0) shards (no flat buffer, no padding).
+
+        params: list of dicts with 'dim0', 'row', 'grads' ((n_ranks, numel)
+        uint16: every rank's full gradient of the parameter) and 'master', 'm',
+        'v': lists over ranks of float32 arrays holding that rank's rows (ragged,
+        possibly empty), updated in place.  For each parameter and rank: the
+        mean over ranks of the gradient rows the rank owns, AdamW on its fp32
+        shard, bf16 cast; the gathered parameter is the concatenation of the
+        ranks' shards in rank order.  Returns the list of (numel,) uint16.
+        """
+        outs = []
+        for prm in params:
+            grads = _u16(prm["grads"])
+            n_ranks, numel = grads.shape
+            full = np.empty(numel, dtype=np.uint16)
+            for r in range(n_ranks):
+                b, e = self.param_shard_bounds(prm["dim0"], prm["row"], n_ranks, r)
+                if e <= b:
+                    continue
+                g = self.rank_mean(np.ascontiguousarray(grads[:, b:e]))
+                self.adamw(prm["master"][r], prm["m"][r], prm["v"][r], g, lr=lr, beta1=beta1,
+                           beta2=beta2, eps=eps, weight_decay=weight_decay, step=step)
+                full[b:e] = self.round_to_bf16(prm["master"][r])
+            outs.append(full)
+        return outs
 
     # -- ZeRO-1 local accumulation ---------------------------------------
     def zero1_accumulate(self, grads, acc_full, first: bool) -> None:

@@ -230,6 +230,32 @@ void oracle_adamw(float* theta, float* m, float* v, const float* g, int64_t n, d
     }
 }
 
+/* ------------------------------------ FSDP2 per-parameter Shard(0) ------- */
+
+/*
+ * FSDP2 per-parameter sharding ([L5] section 7.2: every parameter keeps its
+ * own shape and is split along dim 0 over the data-parallel ranks, with no
+ * FlatParameter and no padding; [A03] section 4; [LA] section 9.5).  Reading:
+ * the rows are split the way a tensor is cut into n_ranks chunks -- chunk =
+ * ceil(dim0 / n_ranks) rows, rank r owns rows [r*chunk, min((r+1)*chunk, dim0))
+ * (possibly none).  Returns the element range [*begin, *end) of rank r.
+ */
+void oracle_param_shard_bounds(int64_t dim0, int64_t row_numel, int32_t n_ranks, int32_t rank,
+                               int64_t* begin, int64_t* end)
+{
+    int64_t chunk = (dim0 + n_ranks - 1) / n_ranks;
+    int64_t first_row = (int64_t)rank * chunk;
+    int64_t last_row = first_row + chunk;
+    if (first_row > dim0) {
+        first_row = dim0;
+    }
+    if (last_row > dim0) {
+        last_row = dim0;
+    }
+    *begin = first_row * row_numel;
+    *end = last_row * row_numel;
+}
+
 /* ------------------------------------- ZeRO-1 local accumulation --------- */
 
 /*

@@ -525,6 +525,56 @@ def check_zero1_accumulation(o):
     assert np.array_equal(ma.view(np.uint32), mb.view(np.uint32))
 
 
+def check_param_shard_bounds_vs_torch_chunk(o):
+    """Per-parameter Shard(0): each rank's rows are the chunk torch.chunk gives
+    (a library routine), in order, with no padding; chunks past the end are empty."""
+    for dim0 in (1, 2, 3, 5, 7, 8, 9, 64, 65, 100, 4096):
+        for n_ranks in (1, 2, 3, 4, 8, 64):
+            for row in (1, 3, 768):
+                sizes = [len(c) for c in torch.arange(dim0).chunk(n_ranks)]
+                sizes += [0] * (n_ranks - len(sizes))
+                prev = 0
+                for r in range(n_ranks):
+                    b, e = o.param_shard_bounds(dim0, row, n_ranks, r)
+                    assert b == prev and e - b == sizes[r] * row
+                    prev = e
+                assert prev == dim0 * row
+
+
+def check_param_sharded_step_equals_flat(o):
+    """Per-parameter sharding changes which rank updates which element, not
+    the update: the gathered parameters equal the unsharded (DDP) step on the
+    same flat vector, bit for bit."""
+    rng = np.random.default_rng(15)
+    shapes = [(5, 3), (64, 7), (1, 11), (9, 1), (130, 2)]
+    for n_ranks in (1, 3, 4, 8):
+        params, flat_g, flat_t = [], [], []
+        for (d0, row) in shapes:
+            n = d0 * row
+            g = random_bf16(rng, (n_ranks, n), 1e-2)
+            t0 = rng.normal(0, 0.02, n).astype(np.float32)
+            prm = dict(dim0=d0, row=row, grads=g, master=[], m=[], v=[])
+            for r in range(n_ranks):
+                b, e = o.param_shard_bounds(d0, row, n_ranks, r)
+                prm["master"].append(t0[b:e].copy())
+                prm["m"].append(np.zeros(e - b, np.float32))
+                prm["v"].append(np.zeros(e - b, np.float32))
+            params.append(prm)
+            flat_g.append(g)
+            flat_t.append(t0)
+        for t in (1, 2):
+            outs = o.param_sharded_step(params, step=t, **HP)
+            if t == 1:
+                G = np.ascontiguousarray(np.concatenate(flat_g, axis=1))
+                theta = np.concatenate(flat_t)
+                mm, vv = np.zeros_like(theta), np.zeros_like(theta)
+                ref = o.ddp_step(G, theta, mm, vv, step=1, **HP)
+                assert np.array_equal(np.concatenate(outs), ref)
+        # the shards hold exactly the parameter's elements: no padding anywhere
+        for prm, (d0, row) in zip(params, shapes):
+            assert sum(len(x) for x in prm["master"]) == d0 * row
+
+
 ALL_CHECKS = [
     check_bf16_rounding,
     check_bf16_widening,
@@ -545,4 +595,6 @@ ALL_CHECKS = [
     check_clip_closed_forms,
     check_clipped_units_step_vs_torch,
     check_zero1_accumulation,
+    check_param_shard_bounds_vs_torch_chunk,
+    check_param_sharded_step_equals_flat,
 ]

@@ -44,6 +44,9 @@ MUTANTS = {
     "zero1_accum_not_reset": ("double prev = first ? 0.0 : (double)acc_full[idx];",
                               "double prev = (double)acc_full[idx];"),
     "zero1_no_micro_average": ("g[e] = (float)((double)mean / (double)n_micro);", "g[e] = mean;"),
+    "fsdp2_floor_chunk": ("int64_t chunk = (dim0 + n_ranks - 1) / n_ranks;",
+                          "int64_t chunk = dim0 / n_ranks + (dim0 % n_ranks > 1);"),
+    "fsdp2_rows_not_scaled": ("*begin = first_row * row_numel;", "*begin = first_row;"),
     "decay_after_update": ("double updated = decayed - lr * m_hat / (sqrt(v_hat) + eps);",
                            "double updated = ((double)theta[i] - lr * m_hat / (sqrt(v_hat) + eps)) * (1.0 - lr * weight_decay * 1.5);"),
 }
