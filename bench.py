@@ -183,12 +183,16 @@ UNITS_PER_LAUNCH = 32
 POINTERS_PER_LAUNCH = 3712
 
 
-def staged_launches(n_ranks_per_unit, n_out=1):
+def staged_launches(n_ranks_per_unit, n_out=1, pointers=None):
+    """Launches zero_step_units issues for these units; `pointers(n)` is the
+    pointer count one unit of n ranks needs (default: a plain fused step)."""
     if os.environ.get("ZERO_STEP_KERNEL") == "direct":
         return len(n_ranks_per_unit)        # the direct-load kernels: one launch per unit
+    if pointers is None:
+        pointers = lambda n: 4 * n + n_out
     launches, units, ptrs = 0, 0, 0
     for n in n_ranks_per_unit:
-        need = 4 * n + n_out
+        need = pointers(n)
         if units == UNITS_PER_LAUNCH or ptrs + need > POINTERS_PER_LAUNCH or units == 0:
             launches += 1
             units, ptrs = 0, 0
@@ -197,10 +201,16 @@ def staged_launches(n_ranks_per_unit, n_out=1):
     return launches
 
 
-def unit_bytes(P_pad, n_ranks, n_out=1):
-    """Algorithmic HBM bytes of one fused launch: each gradient, state and
-    parameter byte crosses HBM exactly once."""
-    return P_pad * (2 * n_ranks + 24 + 2 * n_out)
+def unit_bytes(P_pad, n_ranks, n_out=1, n_micro=1):
+    """Algorithmic HBM bytes of one optimizer step of one unit: each gradient,
+    state and parameter byte crosses HBM exactly once.  With K > 1 micro-steps:
+    the first reduce-scatter writes the fp32 accumulator (2N + 4 per element),
+    the middle ones read and write it (2N + 8), the fused last one reads it
+    with the state (2N + 4 + 24 + 2 n_out)."""
+    if n_micro <= 1:
+        return P_pad * (2 * n_ranks + 24 + 2 * n_out)
+    per = (2 * n_ranks + 4) + (n_micro - 2) * (2 * n_ranks + 8) + (2 * n_ranks + 28 + 2 * n_out)
+    return P_pad * per
 
 
 class Resident:
@@ -216,8 +226,10 @@ class Resident:
         units = w.units if n_units is None else w.units[:n_units]
         self.units = []
         shared = None
+        self.n_micro = w.n_micro
         for ui, u in enumerate(units):
-            fu = FlatUnit(u.numels, w.n_ranks, with_grads=not (shared_grads and shared is not None))
+            fu = FlatUnit(u.numels, w.n_ranks, accum=w.n_micro > 1,
+                          with_grads=not (shared_grads and shared is not None))
             if shared_grads:
                 if shared is None:
                     shared = fu.grads
@@ -235,19 +247,28 @@ class Resident:
             self.units.append(fu)
         torch.cuda.synchronize()
         self.numel = sum(fu.P for fu in self.units)
-        self.bytes = sum(unit_bytes(fu.P_pad, w.n_ranks) for fu in self.units)
-        self.ptrs = [(fu.grad_rows(), *fu.state_rows(), None, fu.param_rows(), fu.layout)
-                     for fu in self.units]
-        self.launches_per_step = staged_launches([fu.n_ranks for fu in self.units], n_out=1)
+        self.bytes = sum(unit_bytes(fu.P_pad, w.n_ranks, n_micro=w.n_micro) for fu in self.units)
+        self.ptrs = [(fu.grad_rows(), *fu.state_rows(), fu.accum_rows(), fu.param_rows(),
+                      fu.layout) for fu in self.units]
+        from fsdp_sharded_mixed_flatten_gb300.zero import prepare_units
+        self.prepared = prepare_units(self.ptrs)      # pointer tables marshalled once
+        nr = [fu.n_ranks for fu in self.units]
+        if w.n_micro > 1:
+            self.launches_per_step = (
+                (w.n_micro - 1) * staged_launches(nr, pointers=lambda n: 2 * n)
+                + staged_launches(nr, pointers=lambda n: 5 * n + 1))
+        else:
+            self.launches_per_step = staged_launches(nr, n_out=1)
 
     def launch(self, step, hp_base, events=None):
-        """One optimizer step over every unit: a single zero_step_units call
-        (the library packs the units into as few launches as it can)."""
+        """One optimizer step over every unit: one zero_step_units call per
+        micro-step (the library packs the units into as few launches as it can)."""
         from fsdp_sharded_mixed_flatten_gb300 import zero_step_units
         hp = dict(hp_base, step=step)
         if events is not None:
             events[0][0].record()
-        zero_step_units(self.ptrs, 1, 1, hp)
+        for k in range(1, self.n_micro + 1):
+            zero_step_units(self.prepared, k, self.n_micro, hp)
         if events is not None:
             events[0][1].record()
         return self.launches_per_step
@@ -299,10 +320,23 @@ def time_e2e(res, steps, warmup, ws, device):
     d2h = sum(x.numel() * 2 for x in host_p)
     from fsdp_sharded_mixed_flatten_gb300 import zero_step_units
 
+    # The host->device copies are spread over several streams (one per copy
+    # engine) by gradient row; the step waits for all of them.
+    cur = torch.cuda.current_stream()
+    copy_streams = [torch.cuda.Stream() for _ in range(4)]
+    rows_h2d = [(fu.grads[r], hg[r]) for fu, hg in zip(res.units, host_g)
+                for r in range(fu.grads.shape[0])]
+
     def one(step):
-        for fu, hg in zip(res.units, host_g):
-            fu.grads.copy_(hg, non_blocking=True)
-        zero_step_units(res.ptrs, 1, 1, dict(hp, step=step))
+        ready = cur.record_event()          # the previous step has finished reading grads
+        for s in copy_streams:
+            s.wait_event(ready)
+        for i, (dst, src) in enumerate(rows_h2d):
+            with torch.cuda.stream(copy_streams[i % len(copy_streams)]):
+                dst.copy_(src, non_blocking=True)
+        for s in copy_streams:
+            cur.wait_stream(s)
+        zero_step_units(res.prepared, 1, 1, dict(hp, step=step))
         for fu, hpar in zip(res.units, host_p):
             hpar.copy_(fu.params, non_blocking=True)
 
@@ -392,6 +426,117 @@ def secondary(name, steps, warmup, ws, device, hbm_peak, shared=False, n_units=N
     return out
 
 
+def run_sweep(args, device, hbm_peak):
+    """Flat sizes 4^k and 4^k + 13 (k = 10..15) x N_d in {2, 8, 64}: the fused
+    step (zero_step) against the unfused reduce-scatter + AdamW + all-gather
+    sequence, one JSON line per point.  Points whose step moves less than
+    4 x L2 (129 MB) stay partly cache-resident between steps and are marked."""
+    import gc
+    import torch
+    import fsdp_sharded_mixed_flatten_gb300 as zf
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    from fsdp_sharded_mixed_flatten_gb300.buffers import aligned_rows, rows
+    hp0 = dict(synthetic.ADAMW_DEFAULTS)
+    sizes = synthetic.sweep_sizes() if not args.sweep_sizes else \
+        [int(x) for x in args.sweep_sizes.split(",")]
+    for P in sizes:
+        for n in synthetic.SWEEP_RANKS:
+            w = synthetic.workload(f"sweep:{P}:{n}")
+            res = Resident(w)
+            fu = res.units[0]
+            steps = int(max(3, min(200, 2e10 // res.bytes)))
+            el, kern, _, _ = time_resident(res, steps, 3, 1, device)
+            fused_gbs = res.bytes * steps / kern / 1e9
+            gsh = aligned_rows(n, fu.S, torch.float32, device, 0)
+            psh = aligned_rows(n, fu.S, torch.bfloat16, device, 0)
+            master, m, v = fu.state_rows()
+
+            def unfused(t):
+                hp = dict(hp0, step=t)
+                zf.zero_reduce_scatter(fu.grad_rows(), rows(gsh), fu.layout, 0)
+                zf.zero_adamw_shard_step(master, m, v, rows(gsh), 1.0, rows(psh), fu.layout, hp)
+                zf.zero_all_gather(rows(psh), fu.param_rows(), fu.layout)
+
+            for t in range(1, 4):
+                unfused(1000 + t)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            for t in range(steps):
+                unfused(2000 + t)
+            b.record()
+            torch.cuda.synchronize()
+            un_el = a.elapsed_time(b) / 1e3
+            un_bytes = fu.P_pad * (2 * n + 38)
+            line = {"sweep": True, "P": P, "n_ranks": n, "P_pad": fu.P_pad, "S": fu.S,
+                    "S_mod_8": fu.S % 8, "steps": steps,
+                    "fused_bytes_per_step": res.bytes, "fused_ms": kern / steps * 1e3,
+                    "fused_gbs": fused_gbs, "fused_frac_of_measured_hbm": fused_gbs / hbm_peak,
+                    "unfused_bytes_per_step": un_bytes, "unfused_ms": un_el / steps * 1e3,
+                    "unfused_gbs": un_bytes * steps / un_el / 1e9,
+                    "unfused_frac_of_measured_hbm": un_bytes * steps / un_el / 1e9 / hbm_peak,
+                    "fused_speedup": un_el / kern,
+                    "l2_resident": res.bytes < 4 * 129e6}
+            print(json.dumps(line), flush=True)
+            del res, fu, gsh, psh, master, m, v
+            gc.collect()
+            torch.cuda.empty_cache()
+    return 0
+
+
+def zero1_vs_zero2(device, hbm_peak, n_micro=4, steps=2):
+    """One optimizer step of K = 4 micro-batches on the Llama-3-8B layer
+    (N_d = 64) in the ZeRO-2 form (reduce-scatter into the sharded fp32
+    accumulator every micro-step, fused last step) and in the ZeRO-1 form
+    (each rank accumulates its full fp32 gradient locally, one reduce-scatter
+    at the end).  Both are timed with CUDA events; bytes are algorithmic."""
+    import gc
+    import torch
+    import fsdp_sharded_mixed_flatten_gb300 as zf
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    from fsdp_sharded_mixed_flatten_gb300.buffers import FlatUnit, aligned_rows, rows
+    w = synthetic.workload("llama3-8b-layer")
+    u = FlatUnit(w.units[0].numels, w.n_ranks, accum=True)
+    for r in range(w.n_ranks):
+        synthetic.fill_grad_(u.grads[r], u.P, w.grad_std, synthetic.seed_for("z1z2", r))
+    full_acc = aligned_rows(w.n_ranks, u.P_pad, torch.float32, device, 0)
+    hp = dict(synthetic.ADAMW_DEFAULTS)
+    N, P_pad = w.n_ranks, u.P_pad
+
+    def zero2(t):
+        for k in range(1, n_micro + 1):
+            zf.zero_step(u.grad_rows(), *u.state_rows(), u.accum_rows(), k, n_micro,
+                         u.param_rows(), u.layout, dict(hp, step=t))
+
+    def zero1(t):
+        for k in range(1, n_micro + 1):
+            zf.zero1_accumulate(u.grad_rows(), rows(full_acc), k == 1, u.layout)
+        zf.zero1_step(rows(full_acc), n_micro, *u.state_rows(), u.param_rows(), u.layout,
+                      dict(hp, step=t))
+
+    out = {}
+    b2 = unit_bytes(P_pad, N, n_micro=n_micro)
+    b1 = P_pad * N * (6 + 10 * (n_micro - 1)) + P_pad * (4 * N + 26)
+    for name, fn, nbytes in (("zero2", zero2, b2), ("zero1", zero1, b1)):
+        for t in range(1, 3):
+            fn(t)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for t in range(steps):
+            fn(100 + t)
+        b.record()
+        torch.cuda.synchronize()
+        el = a.elapsed_time(b) / 1e3 / steps
+        out[name] = {"ms_per_step": el * 1e3, "bytes_per_step": nbytes,
+                     "gbs": nbytes / el / 1e9, "frac_of_measured_hbm": nbytes / el / 1e9 / hbm_peak}
+    out["zero1_over_zero2_time"] = out["zero1"]["ms_per_step"] / out["zero2"]["ms_per_step"]
+    del u, full_acc
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args, ws, rank, local):
     import torch
     if not torch.cuda.is_available():
@@ -403,6 +548,8 @@ def run_ours(args, ws, rank, local):
     from fsdp_sharded_mixed_flatten_gb300 import synthetic
     zf.load()   # fails loudly if the CUDA library was not built
     hbm_peak, peak_kind = peaks()
+    if args.sweep:
+        return run_sweep(args, device, hbm_peak)
 
     w = synthetic.workload(args.workload)
     res = Resident(w)
@@ -430,6 +577,10 @@ def run_ours(args, ws, rank, local):
                                                           hbm_peak)
         extra["7.5B-32units-Nd64-streamed-grads"] = secondary("7.5b", 2, 1, ws, device,
                                                               hbm_peak, shared=True)
+        extra["7.5B-32units-Nd64-fp32-accum-4-micro"] = secondary("7.5b-accum", 2, 1, ws, device,
+                                                                  hbm_peak, shared=True)
+
+        extra["llama3-8b-layer-K4-zero2-vs-zero1"] = zero1_vs_zero2(device, hbm_peak)
 
     base = cpu_baseline() if (rank == 0 and ws == 1 and not args.no_cpu) else None
     line = {
@@ -476,6 +627,9 @@ def main():
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--sweep", action="store_true",
+                    help="fused vs unfused over the flat-size x N_d sweep (JSON line per point)")
+    ap.add_argument("--sweep-sizes", default="", help="comma-separated flat sizes for --sweep")
     args = ap.parse_args()
     if args.workload not in WORKLOAD_NAMES and not args.workload.startswith("sweep:"):
         ap.error(f"unknown workload {args.workload}")

@@ -6,14 +6,15 @@ The compute lives in the CUDA library declared by ``include/zero_flat.h``;
 out per-rank device buffers with PyTorch allocations, ``synthetic`` draws the
 seeded synthetic workloads, and ``build`` compiles the library in-tree.
 """
-from .zero import (ZERO_MAX_RANKS, ZeroAdamW, ZeroError, ZeroLayout, load, zero_abi_version,
+from .zero import (ZERO_MAX_RANKS, zero1_accumulate, zero1_step, zero_param_layout,
+                   zero_shard_numel, ZeroAdamW, ZeroError, ZeroLayout, load, zero_abi_version,
                    zero_adamw_shard_step, zero_all_gather, zero_device_status, zero_flat_layout,
                    zero_flatten, zero_last_error, zero_reduce_scatter, zero_selftest_wait_timeout,
                    zero_shard_segments, zero_step, zero_step_units, zero_step_units_clip,
                    zero_step_units_clip_noalloc, zero_clip_workspace_bytes, zero_unflatten)
 
 __all__ = [
-    "ZERO_MAX_RANKS", "ZeroAdamW", "ZeroError", "ZeroLayout", "load", "zero_abi_version",
+    "ZERO_MAX_RANKS", "zero1_accumulate", "zero1_step", "zero_param_layout", "zero_shard_numel", "ZeroAdamW", "ZeroError", "ZeroLayout", "load", "zero_abi_version",
     "zero_adamw_shard_step", "zero_all_gather", "zero_device_status", "zero_flat_layout",
     "zero_flatten",
     "zero_last_error", "zero_reduce_scatter", "zero_selftest_wait_timeout",

@@ -42,6 +42,8 @@ int ok() {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+bool unpadded(const zero_layout_t* L) { return (L->flags & ZERO_LAYOUT_UNPADDED) != 0; }
+
 int check_layout(const zero_layout_t* L) {
     if (L == nullptr) return fail(ZERO_ERR_INVALID_ARG, "layout is NULL");
     if (L->n_ranks < 1) return fail(ZERO_ERR_INVALID_ARG, "n_ranks = %d < 1", L->n_ranks);
@@ -49,14 +51,26 @@ int check_layout(const zero_layout_t* L) {
         return fail(ZERO_ERR_SIZE, "n_ranks = %d exceeds %d", L->n_ranks, ZERO_MAX_RANKS);
     if (L->numel < 1) return fail(ZERO_ERR_INVALID_ARG, "numel = %lld < 1", (long long)L->numel);
     if (L->n_tensors < 1) return fail(ZERO_ERR_INVALID_ARG, "n_tensors < 1");
+    if (L->flags != 0 && L->flags != ZERO_LAYOUT_UNPADDED)
+        return fail(ZERO_ERR_INVALID_ARG, "unknown layout flags %d", L->flags);
     if (L->shard_numel < 1 || L->numel_padded / L->n_ranks != L->shard_numel ||
         L->numel_padded % L->n_ranks != 0)
         return fail(ZERO_ERR_SIZE, "numel_padded != n_ranks * shard_numel");
-    if (L->numel_padded < L->numel || L->numel_padded - L->numel >= L->n_ranks)
+    if (L->numel_padded < L->numel)
+        return fail(ZERO_ERR_SIZE, "numel_padded < numel");
+    if (!unpadded(L) && L->numel_padded - L->numel >= L->n_ranks)
         return fail(ZERO_ERR_SIZE, "numel_padded is not numel rounded up to a multiple of n_ranks");
     const int64_t tiles = (L->shard_numel + zf::kTile - 1) / zf::kTile;
     if (tiles * L->n_ranks > std::numeric_limits<int32_t>::max())
         return fail(ZERO_ERR_SIZE, "flat buffer too large");
+    return ZERO_OK;
+}
+
+// Entry points that only handle FlatParameter (padded) layouts.
+int check_padded(const zero_layout_t* L, const char* what) {
+    if (int rc = check_layout(L)) return rc;
+    if (unpadded(L))
+        return fail(ZERO_ERR_INVALID_ARG, "%s does not take unpadded per-parameter layouts", what);
     return ZERO_OK;
 }
 
@@ -156,9 +170,10 @@ struct UnitView {
 
 bool mode_reads_grads(int mode) { return mode != zf::kModeFromShard; }
 bool mode_updates(int mode) {
-    return mode == zf::kModePlain || mode == zf::kModeAccumFinal || mode == zf::kModeFromShard;
+    return mode == zf::kModePlain || mode == zf::kModeAccumFinal || mode == zf::kModeFromShard ||
+           mode == zf::kModeMeanDiv;
 }
-bool mode_uses_accum(int mode) { return mode != zf::kModePlain; }
+bool mode_uses_accum(int mode) { return mode != zf::kModePlain && mode != zf::kModeMeanDiv; }
 
 int pointers_needed(const UnitView& u, int mode) {
     const int n = u.L->n_ranks;
@@ -184,33 +199,37 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
                         cudaStream_t stream, ClipPlan* clip = nullptr) {
     static thread_local zf::MultiArgs a;
     int np = 0;
-    a.n_units = 0;
-    a.total_tiles = 0;
-    a.k = k;
+    a.h.n_units = 0;
+    a.h.total_tiles = 0;
+    a.h.k = k;
     auto flush = [&]() -> int {
-        if (a.n_units == 0) return ZERO_OK;
+        if (a.h.n_units == 0) return ZERO_OK;
         int rc = ZERO_OK;
         if (clip != nullptr) {
-            a.partials = clip->partials;
-            a.partial_base = static_cast<int32_t>(clip->slots_used);
-            a.n_partials = clip->n_partials;
-            a.max_norm = clip->max_norm;
-            a.norm_out = clip->norm_out;
+            a.h.partials = clip->partials;
+            a.h.partial_base = static_cast<int32_t>(clip->slots_used);
+            a.h.n_partials = clip->n_partials;
+            a.h.max_norm = clip->max_norm;
+            a.h.norm_out = clip->norm_out;
             if (mode == zf::kModeRsNorm || mode == zf::kModeRsAvgNorm) {
-                const int grid = zf::staged_grid(mode, a.total_tiles);
+                const int grid = zf::staged_grid(mode, a.h.total_tiles);
                 if (clip->slots_used + grid > clip->capacity && !clip->dry_run)
                     return fail(ZERO_ERR_SIZE, "clipping workspace too small: need %lld slots",
                                 (long long)(clip->slots_used + grid));
                 clip->slots_used += grid;
             }
         } else {
-            a.partials = nullptr;
-            a.norm_out = nullptr;
+            a.h.partials = nullptr;
+            a.h.norm_out = nullptr;
         }
-        if (clip == nullptr || !clip->dry_run)
-            rc = cuda_status(zf::launch_staged_step(a, mode, stream), "staged step launch");
-        a.n_units = 0;
-        a.total_tiles = 0;
+        if (clip == nullptr || !clip->dry_run) {
+            const cudaError_t e = mode == zf::kModeMeanDiv
+                                      ? zf::launch_staged_step_f32(a, np, stream)
+                                      : zf::launch_staged_step(a, np, mode, stream);
+            rc = cuda_status(e, "staged step launch");
+        }
+        a.h.n_units = 0;
+        a.h.total_tiles = 0;
         np = 0;
         return rc;
     };
@@ -220,16 +239,17 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
         const int need = pointers_needed(u, mode);
         const int64_t tpr = (u.L->shard_numel + zf::kStagedTile - 1) / zf::kStagedTile;
         const int64_t tiles = tpr * n;
-        if (a.n_units == zf::kMaxUnits || np + need > zf::kMaxPtrs ||
-            static_cast<int64_t>(a.total_tiles) + tiles > std::numeric_limits<int32_t>::max()) {
+        if (a.h.n_units == zf::kMaxUnits || np + need > zf::kMaxPtrs ||
+            static_cast<int64_t>(a.h.total_tiles) + tiles > std::numeric_limits<int32_t>::max()) {
             if (int rc = flush()) return rc;
         }
-        zf::UnitDesc& d = a.unit[a.n_units];
+        zf::UnitDesc& d = a.unit[a.h.n_units];
         d.S = u.L->shard_numel;
         d.P_pad = u.L->numel_padded;
+        d.P_valid = unpadded(u.L) ? u.L->numel : u.L->numel_padded;
         d.n_ranks = n;
         d.n_out = 0;
-        d.tile_begin = a.total_tiles;
+        d.tile_begin = a.h.total_tiles;
         d.tiles_per_rank = static_cast<int32_t>(tpr);
         d.n_ranks_f = static_cast<float>(n);
         d.inv_n = static_cast<float>(1.0 / static_cast<double>(n));
@@ -254,8 +274,8 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
             d.off_accum = np;
             for (int r = 0; r < n; ++r) a.ptrs[np++] = u.accum[r];
         }
-        a.total_tiles += static_cast<int32_t>(tiles);
-        a.n_units += 1;
+        a.h.total_tiles += static_cast<int32_t>(tiles);
+        a.h.n_units += 1;
     }
     return flush();
 }
@@ -340,6 +360,12 @@ int run_units(const UnitView* units, int n_units, int32_t micro_step, int32_t n_
         return launch_units_staged(units, n_units, mode, k, stream);
     }
     for (int i = 0; i < n_units; ++i) {
+        if (unpadded(units[i].L))
+            return fail(ZERO_ERR_INVALID_ARG,
+                        "unpadded per-parameter layouts need the staged kernels "
+                        "(ZERO_STEP_KERNEL=direct is set)");
+    }
+    for (int i = 0; i < n_units; ++i) {
         const UnitView& u = units[i];
         const int need = u.L->n_ranks > (optimizer_runs ? u.n_out : 0) ? u.L->n_ranks : u.n_out;
         const int rc = need <= 64 ? run_step_direct<64>(u, micro_step, n_micro, hp, stream)
@@ -380,7 +406,7 @@ ZERO_API int zero_flat_layout(const int64_t* numels, int64_t n_tensors, int32_t 
     layout_out->shard_numel = shard;
     layout_out->numel_padded = shard * n_ranks;
     layout_out->n_ranks = n_ranks;
-    layout_out->reserved = 0;
+    layout_out->flags = 0;
     return ok();
 }
 
@@ -388,7 +414,7 @@ ZERO_API int zero_shard_segments(const zero_layout_t* L, const int64_t* offsets,
                                  const int64_t* numels, int32_t rank, int64_t* seg_tensor,
                                  int64_t* seg_begin, int64_t* seg_end, int64_t cap,
                                  int64_t* n_seg) {
-    if (int rc = check_layout(L)) return rc;
+    if (int rc = check_padded(L, "zero_shard_segments")) return rc;
     if (offsets == nullptr || numels == nullptr || n_seg == nullptr)
         return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
     if (cap > 0 && (seg_tensor == nullptr || seg_begin == nullptr || seg_end == nullptr))
@@ -432,7 +458,7 @@ ZERO_API int zero_shard_segments(const zero_layout_t* L, const int64_t* offsets,
 static int flatten_impl(const void* const* tensors, const int64_t* offsets, const int64_t* numels,
                         int32_t elem_bytes, void* const* flat, int32_t split,
                         const zero_layout_t* L, void* stream, int unflatten) {
-    if (int rc = check_layout(L)) return rc;
+    if (int rc = check_padded(L, "zero_flatten / zero_unflatten")) return rc;
     if (tensors == nullptr || offsets == nullptr || numels == nullptr || flat == nullptr)
         return fail(ZERO_ERR_INVALID_ARG, "NULL argument");
     if (elem_bytes != 2 && elem_bytes != 4)
@@ -526,6 +552,8 @@ ZERO_API int zero_reduce_scatter(const uint16_t* const* grads, float* const* gra
         return launch_units_staged(&u, 1, accumulate ? zf::kModeRsAdd : zf::kModeRsStore,
                                    zf::AdamConsts{}, st);
     }
+    if (unpadded(L))
+        return fail(ZERO_ERR_INVALID_ARG, "unpadded layouts need the staged kernels");
     if (n <= 64) return rs_impl<64>(grads, grad_shards, L, accumulate, st);
     return rs_impl<512>(grads, grad_shards, L, accumulate, st);
 }
@@ -555,7 +583,7 @@ ZERO_API int zero_adamw_shard_step(float* const* master, float* const* m, float*
                                    const float* const* grad_shards, float grad_divisor,
                                    uint16_t* const* param_shards, const zero_layout_t* L,
                                    const zero_adamw_t* hp, void* stream) {
-    if (int rc = check_layout(L)) return rc;
+    if (int rc = check_padded(L, "zero_adamw_shard_step")) return rc;
     if (int rc = check_hp(hp)) return rc;
     const int n = L->n_ranks;
     if (int rc = check_ptrs(const_cast<const float* const*>(master), n, "master")) return rc;
@@ -587,7 +615,7 @@ static int gather_impl(const uint16_t* const* param_shards, uint16_t* const* ful
 
 ZERO_API int zero_all_gather(const uint16_t* const* param_shards, uint16_t* const* full_params,
                              int32_t n_out, const zero_layout_t* L, void* stream) {
-    if (int rc = check_layout(L)) return rc;
+    if (int rc = check_padded(L, "zero_all_gather")) return rc;
     if (n_out < 1 || n_out > ZERO_MAX_RANKS)
         return fail(ZERO_ERR_INVALID_ARG, "n_out must lie in [1, %d]", ZERO_MAX_RANKS);
     const int n = L->n_ranks;
@@ -814,4 +842,86 @@ ZERO_API int zero_step_units_clip_noalloc(const zero_unit_t* units, int32_t n_un
     if (int rc = launch_units_staged(views, n_units, norm_mode, k, st, &plan)) return rc;
     plan.n_partials = static_cast<int32_t>(plan.slots_used);
     return launch_units_staged(views, n_units, zf::kModeFromShard, k, st, &plan);
+}
+
+// ------------------------------------------------ ZeRO-1 accumulation ------
+
+ZERO_API int zero1_accumulate(const uint16_t* const* grads, float* const* full_accum,
+                              int32_t first, const zero_layout_t* L, void* stream) {
+    if (int rc = check_padded(L, "zero1_accumulate")) return rc;
+    const int n = L->n_ranks;
+    if (int rc = check_ptrs(grads, n, "grads")) return rc;
+    if (int rc = check_ptrs(const_cast<const float* const*>(full_accum), n, "full_accum"))
+        return rc;
+    if (first != 0 && first != 1) return fail(ZERO_ERR_INVALID_ARG, "first must be 0 or 1");
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    auto go = [&](auto& a) -> int {
+        std::memset(&a, 0, sizeof a);
+        fill_step_args(a, L);
+        for (int k = 0; k < n; ++k) {
+            a.grads[k] = grads[k];
+            a.accum[k] = full_accum[k];
+        }
+        return ZERO_OK;
+    };
+    if (n <= 64) {
+        static thread_local zf::StepArgs<64> a;
+        go(a);
+        return cuda_status(zf::launch_zero1_accumulate<64>(a, first, st), "accumulate launch");
+    }
+    static thread_local zf::StepArgs<512> a;
+    go(a);
+    return cuda_status(zf::launch_zero1_accumulate<512>(a, first, st), "accumulate launch");
+}
+
+ZERO_API int zero1_step(const float* const* full_accum, int32_t n_micro, float* const* master,
+                        float* const* m, float* const* v, uint16_t* const* full_params,
+                        int32_t n_out, const zero_layout_t* L, const zero_adamw_t* hp,
+                        void* stream) {
+    if (int rc = check_padded(L, "zero1_step")) return rc;
+    if (int rc = check_hp(hp)) return rc;
+    if (n_micro < 1) return fail(ZERO_ERR_INVALID_ARG, "n_micro < 1");
+    const int n = L->n_ranks;
+    if (int rc = check_ptrs(full_accum, n, "full_accum")) return rc;
+    // The staged kernel reads the accumulators through the gradient table.
+    const UnitView u{L, reinterpret_cast<const uint16_t* const*>(full_accum), master, m, v,
+                     nullptr, full_params, n_out};
+    if (int rc = check_unit(u, 1, 1, true)) return rc;
+    return launch_units_staged(&u, 1, zf::kModeMeanDiv,
+                               derive_consts(hp, static_cast<double>(n_micro)),
+                               static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------ per-parameter Shard(0) ----
+
+ZERO_API int zero_param_layout(int64_t dim0, int64_t row_numel, int32_t n_ranks,
+                               zero_layout_t* layout_out) {
+    if (layout_out == nullptr) return fail(ZERO_ERR_INVALID_ARG, "layout_out is NULL");
+    if (dim0 < 1 || row_numel < 1 || n_ranks < 1)
+        return fail(ZERO_ERR_INVALID_ARG, "dim0, row_numel and n_ranks must be positive");
+    if (dim0 > std::numeric_limits<int64_t>::max() / row_numel)
+        return fail(ZERO_ERR_SIZE, "numel overflows int64");
+    const int64_t chunk_rows = dim0 / n_ranks + (dim0 % n_ranks != 0 ? 1 : 0);
+    if (chunk_rows > std::numeric_limits<int64_t>::max() / row_numel / n_ranks)
+        return fail(ZERO_ERR_SIZE, "padded size overflows int64");
+    layout_out->n_tensors = 1;
+    layout_out->numel = dim0 * row_numel;
+    layout_out->shard_numel = chunk_rows * row_numel;
+    layout_out->numel_padded = layout_out->shard_numel * n_ranks;
+    layout_out->n_ranks = n_ranks;
+    layout_out->flags = ZERO_LAYOUT_UNPADDED;
+    return ok();
+}
+
+ZERO_API int zero_shard_numel(const zero_layout_t* L, int32_t rank, int64_t* numel_out) {
+    if (int rc = check_layout(L)) return rc;
+    if (numel_out == nullptr) return fail(ZERO_ERR_INVALID_ARG, "numel_out is NULL");
+    if (rank < 0 || rank >= L->n_ranks) return fail(ZERO_ERR_INVALID_ARG, "rank out of range");
+    int64_t n = L->shard_numel;
+    if (unpadded(L)) {
+        const int64_t left = L->numel - static_cast<int64_t>(rank) * L->shard_numel;
+        n = left < 0 ? 0 : (left < n ? left : n);
+    }
+    *numel_out = n;
+    return ok();
 }

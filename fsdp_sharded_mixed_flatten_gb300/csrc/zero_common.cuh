@@ -190,6 +190,53 @@ __device__ __forceinline__ void store_bf16x8(uint16_t* base, int64_t e, int mis,
     }
 }
 
+// Store 8 packed bf16 per lane for a whole warp whose lanes own consecutive
+// 8-element groups starting at flat index e (lane 0) -- e, e+8, ... -- with
+// e mod 8 = mis for every lane.  When mis != 0 the lanes' groups straddle the
+// 16-byte grid: lane l builds the aligned block that holds its last mis
+// elements and lane l+1's first 8-mis (one shuffle per word), so lanes 0..30
+// each issue one aligned 16-byte store; lane 0's leading and lane 31's
+// trailing partial blocks are written element by element.  Every lane of the
+// warp must call this (the shuffles use the full mask).
+template <int MIS>
+__device__ __forceinline__ void store_bf16x8_warp_mis(uint16_t* base, int64_t e, uint4 w,
+                                                      int lane) {
+    uint4 nx;
+    nx.x = __shfl_down_sync(0xFFFFFFFFu, w.x, 1);
+    nx.y = __shfl_down_sync(0xFFFFFFFFu, w.y, 1);
+    nx.z = __shfl_down_sync(0xFFFFFFFFu, w.z, 1);
+    nx.w = __shfl_down_sync(0xFFFFFFFFu, w.w, 1);
+    const uint4 blk = align_shift<8 - MIS>(w, nx);
+    if (lane < 31) *reinterpret_cast<uint4*>(base + e - MIS + 8) = blk;
+    const uint32_t words[4] = {w.x, w.y, w.z, w.w};
+    if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < 8 - MIS; ++t) {
+            base[e + t] = static_cast<uint16_t>(words[t >> 1] >> ((t & 1) * 16));
+        }
+    }
+    if (lane == 31) {
+#pragma unroll
+        for (int t = 8 - MIS; t < 8; ++t) {
+            base[e + t] = static_cast<uint16_t>(words[t >> 1] >> ((t & 1) * 16));
+        }
+    }
+}
+
+__device__ __forceinline__ void store_bf16x8_warp(uint16_t* base, int64_t e, int mis, uint4 w,
+                                                  int lane) {
+    switch (mis) {
+        case 0: *reinterpret_cast<uint4*>(base + e) = w; break;
+        case 1: store_bf16x8_warp_mis<1>(base, e, w, lane); break;
+        case 2: store_bf16x8_warp_mis<2>(base, e, w, lane); break;
+        case 3: store_bf16x8_warp_mis<3>(base, e, w, lane); break;
+        case 4: store_bf16x8_warp_mis<4>(base, e, w, lane); break;
+        case 5: store_bf16x8_warp_mis<5>(base, e, w, lane); break;
+        case 6: store_bf16x8_warp_mis<6>(base, e, w, lane); break;
+        default: store_bf16x8_warp_mis<7>(base, e, w, lane); break;
+    }
+}
+
 // ------------------------------------------------------------- AdamW -------
 //
 // One element of the local shard update: decoupled weight decay, the two

@@ -75,6 +75,7 @@ constexpr int kMaxPtrs = 3712;
 struct UnitDesc {
     int64_t S;
     int64_t P_pad;
+    int64_t P_valid;          // elements the buffers hold: P_pad, or numel when unpadded
     int32_t n_ranks;
     int32_t n_out;
     int32_t tile_begin;       // first tile of this unit in the launch's tile sequence
@@ -90,7 +91,8 @@ struct UnitDesc {
     int32_t n_pow2;
 };
 
-struct MultiArgs {
+// Launch-wide fields of a staged launch.
+struct MultiHeader {
     int32_t n_units;
     int32_t total_tiles;
     AdamConsts k;
@@ -100,9 +102,21 @@ struct MultiArgs {
     int32_t n_partials;     // slots an update launch reduces (fixed order)
     double max_norm;        // clip threshold
     float* norm_out;        // optional: total norm written by CTA 0 of an update launch
-    UnitDesc unit[kMaxUnits];
-    const void* ptrs[kMaxPtrs];
 };
+
+// Argument block of one staged launch, in two capacities: the launch copies
+// the whole block, so small launches use a small one (each launch pays for
+// its argument bytes).
+template <int UNITS, int PTRS>
+struct MultiArgsT {
+    static constexpr int kUnits = UNITS;
+    static constexpr int kPtrs = PTRS;
+    MultiHeader h;
+    UnitDesc unit[UNITS];
+    const void* ptrs[PTRS];
+};
+using MultiArgsS = MultiArgsT<4, 384>;
+using MultiArgs = MultiArgsT<kMaxUnits, kMaxPtrs>;   // the host builds this one
 
 static_assert(sizeof(MultiArgs) <= 32764, "launch argument block limit");
 
@@ -113,7 +127,8 @@ enum StepMode : int {
     kModeRsAdd = 3,       // reduce-scatter: accum += mean
     kModeRsNorm = 4,      // clipping pass 1: accum = mean, per-CTA sum of mean^2
     kModeRsAvgNorm = 5,   // clipping pass 1, last micro-step: accum = (accum + mean) / K, sum
-    kModeFromShard = 6    // clipping pass 2: AdamW from accum * clip coefficient
+    kModeFromShard = 6,   // clipping pass 2: AdamW from accum * clip coefficient
+    kModeMeanDiv = 7      // ZeRO-1 last step: fp32 full accumulators, g = mean / K
 };
 
 // Device-side status codes (g_zf_device_status); must match ZERO_DEVICE_*.
@@ -130,8 +145,16 @@ cudaError_t launch_adamw_shards(const ShardArgs<MAXR>& a, cudaStream_t stream);
 template <int MAXR>
 cudaError_t launch_all_gather(const ShardArgs<MAXR>& a, cudaStream_t stream);
 cudaError_t launch_flatten(const FlatArgs& a, int elem_bytes, int unflatten, cudaStream_t stream);
-// Bulk-copy staged fused step / reduce-scatter over the units of `a` (mode: StepMode).
-cudaError_t launch_staged_step(const MultiArgs& a, int mode, cudaStream_t stream);
+// Bulk-copy staged fused step / reduce-scatter over the units of `a` (mode:
+// StepMode); `n_ptrs` pointers of a.ptrs are in use (picks the block size).
+cudaError_t launch_staged_step(const MultiArgs& a, int n_ptrs, int mode, cudaStream_t stream);
+// The same, reading fp32 gradient buffers (ZeRO-1 full accumulators; mode
+// kModeMeanDiv only).
+cudaError_t launch_staged_step_f32(const MultiArgs& a, int n_ptrs, cudaStream_t stream);
+// ZeRO-1 local accumulation of each rank's bf16 gradient into its full fp32
+// accumulator (a.grads -> a.accum, P_pad elements each).
+template <int MAXR>
+cudaError_t launch_zero1_accumulate(const StepArgs<MAXR>& a, int first, cudaStream_t stream);
 // Grid a staged launch of `mode` over `total_tiles` tiles uses (persistent:
 // at most one CTA per SM); norm launches write this many partial sums.
 int staged_grid(int mode, int total_tiles);

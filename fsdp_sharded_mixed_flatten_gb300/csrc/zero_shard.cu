@@ -170,6 +170,61 @@ cudaError_t launch_flatten(const FlatArgs& a, int elem_bytes, int unflatten, cud
     return cudaGetLastError();
 }
 
+// ZeRO-1 local accumulation: rank k's full fp32 accumulator (P_pad elements)
+// plus its own bf16 gradient, element by element (no exchange between ranks).
+// blockIdx.y is the rank; 8 elements per thread, 16-byte loads and stores.
+template <int MAXR, int FIRST>
+__global__ void __launch_bounds__(kThreads)
+zero1_accumulate_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+    const int k = blockIdx.y;
+    const uint16_t* g = a.grads[k];
+    float* acc = a.accum[k];
+    const int64_t groups = a.P_pad / kVec;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < groups;
+         q += stride) {
+        const uint4 w = ld_stream(g + q * kVec);
+        float x[8];
+        const float2 p0 = bf16x2_to_float2(w.x), p1 = bf16x2_to_float2(w.y);
+        const float2 p2 = bf16x2_to_float2(w.z), p3 = bf16x2_to_float2(w.w);
+        x[0] = p0.x; x[1] = p0.y; x[2] = p1.x; x[3] = p1.y;
+        x[4] = p2.x; x[5] = p2.y; x[6] = p3.x; x[7] = p3.y;
+        if constexpr (!FIRST) {
+            float o[8];
+            ld_f32x8(acc + q * kVec, o);
+#pragma unroll
+            for (int t = 0; t < kVec; ++t) x[t] = __fadd_rn(o[t], x[t]);
+        }
+        st_f32x8(acc + q * kVec, x);
+    }
+    const int64_t tail0 = groups * kVec;
+    if (blockIdx.x == 0 && tail0 + threadIdx.x < a.P_pad) {
+        const int64_t e = tail0 + threadIdx.x;
+        const float x = bf16_to_float(g[e]);
+        acc[e] = FIRST ? x : __fadd_rn(acc[e], x);
+    }
+}
+
+template <int MAXR>
+cudaError_t launch_zero1_accumulate(const StepArgs<MAXR>& a, int first, cudaStream_t stream) {
+    const int64_t groups = a.P_pad / kVec;
+    const void* kfn = first ? reinterpret_cast<const void*>(&zero1_accumulate_kernel<MAXR, 1>)
+                            : reinterpret_cast<const void*>(&zero1_accumulate_kernel<MAXR, 0>);
+    const int64_t want = (groups + kThreads - 1) / kThreads;
+    int gx = persistent_grid(kfn, kThreads, 0, want * a.n_ranks) / a.n_ranks;
+    if (gx < 1) gx = 1;
+    if (gx > want && want > 0) gx = static_cast<int>(want);
+    const dim3 grid(static_cast<unsigned>(gx), static_cast<unsigned>(a.n_ranks));
+    if (first) {
+        zero1_accumulate_kernel<MAXR, 1><<<grid, kThreads, 0, stream>>>(a);
+    } else {
+        zero1_accumulate_kernel<MAXR, 0><<<grid, kThreads, 0, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_zero1_accumulate<64>(const StepArgs<64>&, int, cudaStream_t);
+template cudaError_t launch_zero1_accumulate<512>(const StepArgs<512>&, int, cudaStream_t);
 template cudaError_t launch_adamw_shards<64>(const ShardArgs<64>&, cudaStream_t);
 template cudaError_t launch_adamw_shards<512>(const ShardArgs<512>&, cudaStream_t);
 template cudaError_t launch_all_gather<64>(const ShardArgs<64>&, cudaStream_t);

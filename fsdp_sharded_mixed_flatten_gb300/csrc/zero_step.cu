@@ -16,6 +16,8 @@
 // per rank per warp), cache-streaming.  When r*S is not a multiple of 8 the
 // rank's flat slice is not 16-byte aligned: each thread then reads the two
 // aligned vectors that cover its 8 elements and realigns them in registers.
+#include <mutex>
+
 #include "zero_kernels.cuh"
 
 namespace zf {
@@ -195,14 +197,40 @@ reduce_scatter_kernel(const __grid_constant__ StepArgs<MAXR> a) {
     }
 }
 
+// Resident CTAs per SM for (kernel, threads, smem) on a device, and the SM
+// count, looked up once and cached (the occupancy query is not free).
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t work_ctas) {
-    int dev = 0, sms = 0, per_sm = 0;
+    struct Entry {
+        const void* kernel;
+        int dev, threads;
+        size_t smem;
+        int cap;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int n_cached = 0;
+    int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
-    if (sms < 1) sms = 1;
-    if (per_sm < 1) per_sm = 1;
-    const int64_t cap = static_cast<int64_t>(sms) * per_sm;
+    int cap = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < n_cached; ++i) {
+            const Entry& e = cache[i];
+            if (e.kernel == kernel && e.dev == dev && e.threads == threads && e.smem == smem) {
+                cap = e.cap;
+                break;
+            }
+        }
+        if (cap == 0) {
+            int sms = 0, per_sm = 0;
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+            cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+            if (sms < 1) sms = 1;
+            if (per_sm < 1) per_sm = 1;
+            cap = sms * per_sm;
+            if (n_cached < 64) cache[n_cached++] = Entry{kernel, dev, threads, smem, cap};
+        }
+    }
     const int64_t g = work_ctas < cap ? work_ctas : cap;
     return static_cast<int>(g < 1 ? 1 : g);
 }

@@ -4,16 +4,17 @@
 // Same arithmetic, element order and results as zero_step.cu (bit-identical);
 // what changes is how the bytes reach the SM.  One producer lane per CTA
 // streams every byte a tile reads -- the tile's fp32 state (master, m, v,
-// accumulator) and, eight ranks per stage, the N_d bf16 gradient slices --
+// accumulator) and, eight ranks per stage, the N_d gradient slices (bf16, or
+// fp32 for the ZeRO-1 full accumulators, four per stage) --
 // into a ring of shared-memory stages with cp.async.bulk (the Blackwell TMA
 // engine: plain global->shared copies whose completion is counted in bytes on
 // an mbarrier).  Sixteen consumer warps wait on a stage, read their 8 elements
 // per rank from shared memory, release the stage and finally run AdamW and
 // write the results.  A tile is 4096 elements of one rank's shard of one unit,
-// so every gradient copy is an 8 KB contiguous run of one buffer; the ring
-// keeps up to 3 x 64 KB in flight per SM independently of the consumers'
-// registers, which the direct-load kernel cannot (its in-flight bytes are
-// bounded by the loads it holds in registers).  Measured on GB300: with 8
+// so every gradient copy is an 8 KB contiguous run of one buffer; the ring of
+// 3 x 64 KB stages keeps up to 192 KB in flight per SM independently of the
+// consumers' registers, which the direct-load kernel cannot (its in-flight
+// bytes are bounded by the loads it holds in registers).  Measured on GB300: with 8
 // consumer warps per SM the kernel stayed issue/latency-bound near 70 % of
 // the HBM bandwidth; 16 consumer warps reach it.
 //
@@ -31,6 +32,8 @@
 // that runs out records kDeviceTimeout in g_zf_device_status, tells the rest
 // of the CTA to stop, and the CTA waits (bounded again) for the copies it
 // issued before it returns.
+#include <atomic>
+
 #include "zero_kernels.cuh"
 
 namespace zf {
@@ -42,18 +45,79 @@ namespace {
 constexpr int kConsumerWarps = 16;                     // 512 consumers, 8 elements each
 constexpr int kConsumers = kConsumerWarps * 32;
 constexpr int kTmaThreads = kConsumers + 32;           // + 1 producer warp
-constexpr int kSliceElems = kStagedTile + 8;           // aligned superset of a rank's tile slice
-constexpr int kSliceBytes = kSliceElems * 2;           // 8208
-constexpr int kRanksPerStage = 8;
-constexpr int kStageBytes = kRanksPerStage * kSliceBytes;  // 65664 (>= 4 fp32 state arrays)
-constexpr int kStages = 3;                             // ring depth: 3 x 64 KB per SM
+// Gradient element types the staged kernel reads: bf16 gradients, or the fp32
+// full accumulators of the ZeRO-1 variant.  kAlign elements make 16 bytes,
+// the granularity of a bulk copy.
+template <class GT>
+struct GradTraits;
+template <>
+struct GradTraits<uint16_t> {
+    static constexpr int kAlign = 8;
+    static constexpr int kRanksPerStage = 8;
+    __device__ static float widen(uint16_t x) { return bf16_to_float(x); }
+};
+template <>
+struct GradTraits<float> {
+    static constexpr int kAlign = 4;
+    static constexpr int kRanksPerStage = 4;
+    __device__ static float widen(float x) { return x; }
+};
+// A rank's copied slice of a tile: the tile widened down to the 16-byte grid.
+template <class GT>
+constexpr int slice_bytes() {
+    return (kStagedTile + GradTraits<GT>::kAlign) * static_cast<int>(sizeof(GT));
+}
+constexpr int kSliceBytes = slice_bytes<uint16_t>();      // 8208
+// The ring: 3 stages of 64 KB.  A tile's first stage holds its fp32 state
+// arrays (16 KB each) and, when the whole tile fits, its gradient slices too
+// (lead_ranks); every further stage holds the next 8 ranks' bf16 slices (4
+// fp32 slices).  At N_d = 2 a tile is one stage (three tiles in flight); at
+// N_d = 64 it spans 9.  (A ring of 12 x 16 KB stages was measured: it helped
+// N_d = 2 but the 4x more barrier round trips per tile cost 20 % at N_d >= 8.)
+constexpr int kStageBytes = 8 * kSliceBytes;               // 65664
+constexpr int kStages = 3;
+static_assert(GradTraits<uint16_t>::kRanksPerStage * slice_bytes<uint16_t>() <= kStageBytes &&
+                  GradTraits<float>::kRanksPerStage * slice_bytes<float>() <= kStageBytes,
+              "gradient slices must fit a stage");
 constexpr int kStateArrayBytes = kStagedTile * 4;      // 16384
 constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;       // 0.2 s
 
 static_assert(kConsumers * kVec == kStagedTile, "one thread owns 8 elements of a tile");
-static_assert(4 * kStateArrayBytes <= kStageBytes, "state block must fit one stage");
+static_assert(4 * kStateArrayBytes <= kStageBytes, "the state arrays must fit one stage");
+
+// Ranks whose gradient slices share the first stage of a tile with its NS
+// state arrays.
+template <class GT>
+__host__ __device__ constexpr int first_stage_ranks(int ns) {
+    return (kStageBytes - ns * kStateArrayBytes) / slice_bytes<GT>() <
+                   GradTraits<GT>::kRanksPerStage
+               ? (kStageBytes - ns * kStateArrayBytes) / slice_bytes<GT>()
+               : GradTraits<GT>::kRanksPerStage;
+}
 static_assert(kSliceBytes % 16 == 0, "bulk copies need 16-byte sizes");
+
+// Gradient ranks carried by a tile's first stage.  Without state arrays the
+// first stage is an ordinary gradient stage.  With them, the ranks join the
+// state only in a LEAD launch, one whose every unit has few enough ranks that
+// the whole tile fits that one stage (N_d <= 2 for the plain step): one
+// barrier round trip per tile and up to three tiles in flight.  Otherwise the
+// state travels alone.  The choice is a template parameter: measured on
+// GB300, deciding it per tile at run time cost 2-3 % at N_d = 8 and splitting
+// the ranks unevenly over a tile's stages (2 + 6 at N_d = 8) cost 7 %.
+template <int NS, class GT, bool LEAD>
+__device__ __forceinline__ int lead_ranks(int n_gr) {
+    constexpr int R0 = first_stage_ranks<GT>(NS);
+    if constexpr (NS == 0) return n_gr < R0 ? n_gr : R0;
+    if constexpr (LEAD) return n_gr;
+    return 0;
+}
+
+// Modes whose first stage has room for gradient slices next to the state.
+template <int NS, class GT>
+constexpr bool can_lead() {
+    return NS > 0 && first_stage_ranks<GT>(NS) > 0;
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -118,8 +182,9 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
 }
 
 // Unit of a global tile index: the last unit whose first tile is <= tile.
-__device__ __forceinline__ int find_unit(const MultiArgs& a, int tile) {
-    int lo = 0, hi = a.n_units - 1;
+template <class A>
+__device__ __forceinline__ int find_unit(const A& a, int tile) {
+    int lo = 0, hi = a.h.n_units - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
         if (a.unit[mid].tile_begin <= tile) {
@@ -138,39 +203,45 @@ struct TileGeom {
     int64_t j0;       // first shard-local element of the tile
     int nvalid;       // valid elements in the tile (<= kStagedTile)
     int64_t e0;       // first flat element
-    int mis;          // e0 mod 8
+    int mis;          // e0 mod kAlign (8 for bf16, 4 for fp32 gradients)
     int64_t a0;       // aligned start of every rank's copied slice
-    int64_t a1;       // end of the copied slice (aligned, never past the last full 8-group)
+    int64_t a1;       // end of the copied slice (aligned, never past the last full 16 bytes)
     int state_valid;  // state elements copied (multiple of 4)
 };
 
-__device__ __forceinline__ TileGeom tile_geom(const MultiArgs& a, int tile) {
+template <class A, class GT>
+__device__ __forceinline__ TileGeom tile_geom(const A& a, int tile) {
+    constexpr int64_t AL = GradTraits<GT>::kAlign;
     TileGeom g;
     g.u = &a.unit[find_unit(a, tile)];
     const int local = tile - g.u->tile_begin;
     const int64_t S = g.u->S;
     g.r = local / g.u->tiles_per_rank;
     g.j0 = static_cast<int64_t>(local - g.r * g.u->tiles_per_rank) * kStagedTile;
-    const int64_t rem = S - g.j0;
-    g.nvalid = static_cast<int>(rem < kStagedTile ? rem : kStagedTile);
     g.e0 = static_cast<int64_t>(g.r) * S + g.j0;
-    g.mis = static_cast<int>(g.e0 & 7);
+    // valid elements: the tile, the rank's shard and the buffers all bound it
+    // (an unpadded per-parameter layout ends before its last shards do)
+    int64_t rem = S - g.j0;
+    if (g.u->P_valid - g.e0 < rem) rem = g.u->P_valid - g.e0;
+    g.nvalid = static_cast<int>(rem < kStagedTile ? (rem > 0 ? rem : 0) : kStagedTile);
+    g.mis = static_cast<int>(g.e0 & (AL - 1));
     g.a0 = g.e0 - g.mis;
-    const int64_t a1 = (g.e0 + g.nvalid + 7) & ~static_cast<int64_t>(7);
-    const int64_t floor8 = g.u->P_pad & ~static_cast<int64_t>(7);
-    g.a1 = a1 < floor8 ? a1 : floor8;
+    const int64_t a1 = (g.e0 + g.nvalid + AL - 1) & ~(AL - 1);
+    const int64_t floor_al = g.u->P_valid & ~(AL - 1);
+    g.a1 = a1 < floor_al ? a1 : floor_al;
     if (g.a1 < g.a0) g.a1 = g.a0;
     g.state_valid = g.nvalid & ~3;
     return g;
 }
 
-template <typename T>
-__device__ __forceinline__ T ptr_at(const MultiArgs& a, int index) {
+template <typename T, class A>
+__device__ __forceinline__ T ptr_at(const A& a, int index) {
     return static_cast<T>(const_cast<void*>(a.ptrs[index]));
 }
 
-__device__ __forceinline__ const uint16_t* grad_ptr(const MultiArgs& a, const UnitDesc* u, int k) {
-    return ptr_at<const uint16_t*>(a, u->off_grads + k);
+template <class GT, class A>
+__device__ __forceinline__ const GT* grad_ptr(const A& a, const UnitDesc* u, int k) {
+    return ptr_at<const GT*, A>(a, u->off_grads + k);
 }
 
 // Per mode: how many fp32 state arrays a tile's state block holds (master,
@@ -183,7 +254,7 @@ struct ModeTraits {
         MODE == kModeRsStore || MODE == kModeRsAdd || MODE == kModeRsNorm || MODE == kModeRsAvgNorm;
     static constexpr bool kNorm = MODE == kModeRsNorm || MODE == kModeRsAvgNorm;
     static constexpr bool kReadsGrads = MODE != kModeFromShard;
-    static constexpr int kStateArrays = MODE == kModePlain ? 3
+    static constexpr int kStateArrays = (MODE == kModePlain || MODE == kModeMeanDiv) ? 3
                                         : (MODE == kModeAccumFinal || MODE == kModeFromShard) ? 4
                                         : (MODE == kModeRsAdd || MODE == kModeRsAvgNorm) ? 1
                                                                                         : 0;
@@ -191,28 +262,51 @@ struct ModeTraits {
 
 // State array `array` of rank r (order: master, m, v, accumulator; the
 // reduce-scatter modes only have the accumulator).
-template <int MODE>
-__device__ __forceinline__ float* state_ptr(const MultiArgs& a, const UnitDesc* u, int array,
+template <int MODE, class A>
+__device__ __forceinline__ float* state_ptr(const A& a, const UnitDesc* u, int array,
                                             int r) {
     if constexpr (ModeTraits<MODE>::kReduceScatter) {
-        return ptr_at<float*>(a, u->off_accum + r);
+        return ptr_at<float*, A>(a, u->off_accum + r);
     } else {
         const int off = array == 0 ? u->off_master
                         : array == 1 ? u->off_m
                         : array == 2 ? u->off_v
                                      : u->off_accum;
-        return ptr_at<float*>(a, off + r);
+        return ptr_at<float*, A>(a, off + r);
     }
 }
 
 // Sum up to kRanksPerStage rank slices of one stage into (s, c) for a
 // thread's 8 elements starting A elements into its aligned pair of words.
+// fp32 gradient slices: a thread's 8 values start A words into its three
+// aligned 16-byte words.
+template <int A>
+__device__ __forceinline__ void consume_stage_f32(const uint8_t* stage, int nk, int tid,
+                                                  float2 (&s)[4], float2 (&c)[4]) {
+    constexpr int kSlice = slice_bytes<float>();
+    const uint8_t* base = stage + tid * 32;
+#pragma unroll
+    for (int kk = 0; kk < GradTraits<float>::kRanksPerStage; ++kk) {
+        if (kk < nk) {
+            const float4* p = reinterpret_cast<const float4*>(base + kk * kSlice);
+            const float4 x0 = p[0], x1 = p[1];
+            const float4 x2 = (A != 0) ? p[2] : make_float4(0.f, 0.f, 0.f, 0.f);
+            const float W[12] = {x0.x, x0.y, x0.z, x0.w, x1.x, x1.y, x1.z, x1.w,
+                                 x2.x, x2.y, x2.z, x2.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                two_sum_add2(s[q], c[q], make_float2(W[A + 2 * q], W[A + 2 * q + 1]));
+            }
+        }
+    }
+}
+
 template <int A>
 __device__ __forceinline__ void consume_stage(const uint8_t* stage, int nk, int tid,
                                               float2 (&s)[4], float2 (&c)[4]) {
     const uint8_t* base = stage + tid * 16;
 #pragma unroll
-    for (int kk = 0; kk < kRanksPerStage; ++kk) {
+    for (int kk = 0; kk < GradTraits<uint16_t>::kRanksPerStage; ++kk) {
         if (kk < nk) {
             const uint4* p = reinterpret_cast<const uint4*>(base + kk * kSliceBytes);
             uint4 x = p[0];
@@ -222,49 +316,46 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage, int nk, int 
     }
 }
 
-template <int MODE>
-__device__ void producer_loop(const MultiArgs& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
+template <int MODE, class A, class GT, bool LEAD>
+__device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                               volatile int* abort_flag, uint32_t* issued_out) {
     constexpr int NS = ModeTraits<MODE>::kStateArrays;
+    constexpr int RG = GradTraits<GT>::kRanksPerStage;
+    constexpr int kSlice = slice_bytes<GT>();
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < a.total_tiles; tile += gridDim.x) {
-        const TileGeom g = tile_geom(a, tile);
-        const int n_ranks = g.u->n_ranks;
-        if constexpr (NS > 0) {
-            const uint32_t slot = it % kStages, parity = ((it / kStages) & 1) ^ 1;
-            if (!mbar_wait_bounded(smem_u32(&empty[slot]), parity, abort_flag, kWaitLimitNs)) break;
-            const uint32_t bytes = static_cast<uint32_t>(g.state_valid) * 4;
-            const uint32_t bar = smem_u32(&full[slot]);
-            mbar_arrive_expect_tx(bar, NS * bytes);
-            if (bytes > 0) {
-                const uint32_t dst = smem_u32(smem + slot * kStageBytes);
-#pragma unroll
-                for (int arr = 0; arr < NS; ++arr) {
-                    bulk_copy_g2s(dst + arr * kStateArrayBytes,
-                                  state_ptr<MODE>(a, g.u, arr, g.r) + g.j0, bytes, bar);
-                }
-            }
-            ++it;
-        }
-        const uint32_t gbytes = static_cast<uint32_t>(g.a1 - g.a0) * 2;
-        const int groups =
-            ModeTraits<MODE>::kReadsGrads ? (n_ranks + kRanksPerStage - 1) / kRanksPerStage : 0;
+    for (int tile = blockIdx.x; tile < a.h.total_tiles; tile += gridDim.x) {
+        const TileGeom g = tile_geom<A, GT>(a, tile);
+        if (g.nvalid == 0) continue;      // past the end of an unpadded parameter
+        const int n_ranks = ModeTraits<MODE>::kReadsGrads ? g.u->n_ranks : 0;
+        const uint32_t sbytes = static_cast<uint32_t>(g.state_valid) * 4;
+        const uint32_t gbytes = static_cast<uint32_t>(g.a1 - g.a0) * sizeof(GT);
+        // stage 0: state arrays + ranks [0, r0); then RG ranks per stage
+        const int r0 = lead_ranks<NS, GT, LEAD>(n_ranks);
+        const int n_stages = 1 + (n_ranks - r0 + RG - 1) / RG;
         bool stop = false;
-        for (int grp = 0; grp < groups; ++grp) {
+        for (int st = 0; st < n_stages; ++st) {
             const uint32_t slot = it % kStages, parity = ((it / kStages) & 1) ^ 1;
             if (!mbar_wait_bounded(smem_u32(&empty[slot]), parity, abort_flag, kWaitLimitNs)) {
                 stop = true;
                 break;
             }
-            const int k0 = grp * kRanksPerStage;
-            const int nk = min(kRanksPerStage, n_ranks - k0);
+            const int k0 = st == 0 ? 0 : r0 + (st - 1) * RG;
+            const int nk = st == 0 ? r0 : min(RG, n_ranks - k0);
+            const int ns = st == 0 ? NS : 0;
             const uint32_t bar = smem_u32(&full[slot]);
-            mbar_arrive_expect_tx(bar, nk * gbytes);
+            mbar_arrive_expect_tx(bar, ns * sbytes + nk * gbytes);
+            const uint32_t dst = smem_u32(smem + slot * kStageBytes);
+            if (sbytes > 0) {
+                for (int arr = 0; arr < ns; ++arr) {
+                    bulk_copy_g2s(dst + arr * kStateArrayBytes,
+                                  state_ptr<MODE, A>(a, g.u, arr, g.r) + g.j0, sbytes, bar);
+                }
+            }
             if (gbytes > 0) {
-                const uint32_t dst = smem_u32(smem + slot * kStageBytes);
+                const uint32_t gdst = dst + ns * kStateArrayBytes;
                 for (int kk = 0; kk < nk; ++kk) {
-                    bulk_copy_g2s(dst + kk * kSliceBytes, grad_ptr(a, g.u, k0 + kk) + g.a0, gbytes,
-                                  bar);
+                    bulk_copy_g2s(gdst + kk * kSlice, grad_ptr<GT, A>(a, g.u, k0 + kk) + g.a0,
+                                  gbytes, bar);
                 }
             }
             ++it;
@@ -274,8 +365,8 @@ __device__ void producer_loop(const MultiArgs& a, uint8_t* smem, uint64_t* full,
     *issued_out = it;
 }
 
-template <int MODE>
-__device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t* full,
+template <int MODE, class A, class GT, bool LEAD, bool ALIGNED>
+__device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                               uint64_t* empty, volatile int* abort_flag,
                               unsigned int* consumed_min, float clip_coef, double* warp_sq) {
     constexpr int NS = ModeTraits<MODE>::kStateArrays;
@@ -284,8 +375,10 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
     uint32_t it = 0;
     bool ok = true;
     float sq_s = 0.0f, sq_c = 0.0f;   // compensated sum of squares (norm modes)
-    for (int tile = blockIdx.x; tile < a.total_tiles && ok; tile += gridDim.x) {
-        const TileGeom g = tile_geom(a, tile);
+    constexpr int RG = GradTraits<GT>::kRanksPerStage;
+    for (int tile = blockIdx.x; tile < a.h.total_tiles && ok; tile += gridDim.x) {
+        const TileGeom g = tile_geom<A, GT>(a, tile);
+        if (g.nvalid == 0) continue;      // past the end of an unpadded parameter (uniform)
         const UnitDesc* u = g.u;
         const int n_ranks = u->n_ranks;
         const int first = tid * kVec;
@@ -294,32 +387,7 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
         const int64_t e = g.e0 + first;       // thread's first flat element
 
         float st[NS > 0 ? NS : 1][8];
-        if constexpr (NS > 0) {
-            const uint32_t slot = it % kStages, parity = (it / kStages) & 1;
-            if (!mbar_wait_bounded(smem_u32(&full[slot]), parity, abort_flag, kWaitLimitNs)) {
-                ok = false;
-                break;
-            }
-            const bool from_smem = first + kVec <= g.state_valid;
-#pragma unroll
-            for (int arr = 0; arr < NS; ++arr) {
-                if (from_smem) {
-                    const float4* p = reinterpret_cast<const float4*>(
-                        smem + slot * kStageBytes + arr * kStateArrayBytes + first * 4);
-                    const float4 x0 = p[0], x1 = p[1];
-                    st[arr][0] = x0.x; st[arr][1] = x0.y; st[arr][2] = x0.z; st[arr][3] = x0.w;
-                    st[arr][4] = x1.x; st[arr][5] = x1.y; st[arr][6] = x1.z; st[arr][7] = x1.w;
-                } else {
-                    const float* src = state_ptr<MODE>(a, u, arr, g.r) + j;
-#pragma unroll
-                    for (int t = 0; t < kVec; ++t) st[arr][t] = (t < nv) ? src[t] : 0.0f;
-                }
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
-            ++it;
-        }
-
+        const bool from_smem = first + kVec <= g.state_valid;
         float2 s[4], c[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -327,47 +395,106 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
             c[q] = make_float2(0.0f, 0.0f);
         }
         const bool vec = (nv == kVec) && (e + kVec <= g.a1);
-        const int groups =
-            ModeTraits<MODE>::kReadsGrads ? (n_ranks + kRanksPerStage - 1) / kRanksPerStage : 0;
-        for (int grp = 0; grp < groups; ++grp) {
-            const uint32_t slot = it % kStages, parity = (it / kStages) & 1;
-            if (!mbar_wait_bounded(smem_u32(&full[slot]), parity, abort_flag, kWaitLimitNs)) {
-                ok = false;
-                break;
-            }
-            const int k0 = grp * kRanksPerStage;
-            const int nk = min(kRanksPerStage, n_ranks - k0);
-            const uint8_t* stage = smem + slot * kStageBytes;
+        const int n_gr = ModeTraits<MODE>::kReadsGrads ? n_ranks : 0;
+        // Ranks [k0, k0 + nk) of the tile from one stage into (s, c).
+        auto consume = [&](const uint8_t* stage, int k0, int nk) {
             if (vec) {
-                switch (g.mis) {
-                    case 0: consume_stage<0>(stage, nk, tid, s, c); break;
-                    case 1: consume_stage<1>(stage, nk, tid, s, c); break;
-                    case 2: consume_stage<2>(stage, nk, tid, s, c); break;
-                    case 3: consume_stage<3>(stage, nk, tid, s, c); break;
-                    case 4: consume_stage<4>(stage, nk, tid, s, c); break;
-                    case 5: consume_stage<5>(stage, nk, tid, s, c); break;
-                    case 6: consume_stage<6>(stage, nk, tid, s, c); break;
-                    default: consume_stage<7>(stage, nk, tid, s, c); break;
+                if constexpr (ALIGNED) {
+                    consume_stage<0>(stage, nk, tid, s, c);
+                } else if constexpr (sizeof(GT) == 4) {
+                    switch (g.mis) {
+                        case 0: consume_stage_f32<0>(stage, nk, tid, s, c); break;
+                        case 1: consume_stage_f32<1>(stage, nk, tid, s, c); break;
+                        case 2: consume_stage_f32<2>(stage, nk, tid, s, c); break;
+                        default: consume_stage_f32<3>(stage, nk, tid, s, c); break;
+                    }
+                } else {
+                    switch (g.mis) {
+                        case 0: consume_stage<0>(stage, nk, tid, s, c); break;
+                        case 1: consume_stage<1>(stage, nk, tid, s, c); break;
+                        case 2: consume_stage<2>(stage, nk, tid, s, c); break;
+                        case 3: consume_stage<3>(stage, nk, tid, s, c); break;
+                        case 4: consume_stage<4>(stage, nk, tid, s, c); break;
+                        case 5: consume_stage<5>(stage, nk, tid, s, c); break;
+                        case 6: consume_stage<6>(stage, nk, tid, s, c); break;
+                        default: consume_stage<7>(stage, nk, tid, s, c); break;
+                    }
                 }
             } else if (nv > 0) {
                 // Ragged end: scalar reads from global memory, the same two-sum
                 // lane by lane (element 2q in .x, 2q+1 in .y).
                 for (int kk = 0; kk < nk; ++kk) {
-                    const uint16_t* src = grad_ptr(a, u, k0 + kk) + e;
+                    const GT* src = grad_ptr<GT, A>(a, u, k0 + kk) + e;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
-                        if (2 * q < nv) two_sum_add1(s[q].x, c[q].x, bf16_to_float(src[2 * q]));
+                        if (2 * q < nv) {
+                            two_sum_add1(s[q].x, c[q].x, GradTraits<GT>::widen(src[2 * q]));
+                        }
                         if (2 * q + 1 < nv) {
-                            two_sum_add1(s[q].y, c[q].y, bf16_to_float(src[2 * q + 1]));
+                            two_sum_add1(s[q].y, c[q].y, GradTraits<GT>::widen(src[2 * q + 1]));
                         }
                     }
                 }
             }
+        };
+        // Wait for the ring's next stage; the outcome is made warp-uniform so
+        // that the warp's later shuffles see every lane.
+        auto wait_full = [&]() -> const uint8_t* {
+            const uint32_t slot = it % kStages, parity = (it / kStages) & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[slot]), parity,
+                                                           abort_flag, kWaitLimitNs))) {
+                return nullptr;
+            }
+            return smem + slot * kStageBytes;
+        };
+        auto release = [&]() {
             __syncwarp();
-            if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+            if (lane == 0) mbar_arrive(smem_u32(&empty[it % kStages]));
             ++it;
+        };
+
+        // The tile's first stage: its state arrays, then ranks [0, r0).
+        const int r0 = lead_ranks<NS, GT, LEAD>(n_gr);
+        {
+            const uint8_t* stage = wait_full();
+            if (stage == nullptr) {
+                ok = false;
+                continue;
+            }
+#pragma unroll
+            for (int arr = 0; arr < NS; ++arr) {
+                if (from_smem) {
+                    const float4* p =
+                        reinterpret_cast<const float4*>(stage + arr * kStateArrayBytes + first * 4);
+                    const float4 x0 = p[0], x1 = p[1];
+                    st[arr][0] = x0.x; st[arr][1] = x0.y; st[arr][2] = x0.z; st[arr][3] = x0.w;
+                    st[arr][4] = x1.x; st[arr][5] = x1.y; st[arr][6] = x1.z; st[arr][7] = x1.w;
+                } else {
+                    const float* src = state_ptr<MODE, A>(a, u, arr, g.r) + j;
+#pragma unroll
+                    for (int t = 0; t < kVec; ++t) st[arr][t] = (t < nv) ? src[t] : 0.0f;
+                }
+            }
+            if constexpr (NS == 0 || LEAD) {
+                if (r0 > 0) consume(stage + NS * kStateArrayBytes, 0, r0);
+            }
+            release();
         }
-        if (!ok || nv == 0) continue;
+        // Then RG ranks per stage (none left in a LEAD launch).
+        if constexpr (NS == 0 || !LEAD) {
+            for (int k0 = r0; k0 < n_gr; k0 += RG) {
+                const uint8_t* stage = wait_full();
+                if (stage == nullptr) {
+                    ok = false;
+                    break;
+                }
+                consume(stage, k0, min(RG, n_gr - k0));
+                release();
+            }
+        }
+        // every lane of this warp owns a full group (warp-uniform)
+        const bool warp_full = (first - lane * kVec) + 32 * kVec <= g.nvalid;
+        if (!ok || (nv == 0 && !warp_full)) continue;
 
         float mean[8];
 #pragma unroll
@@ -383,13 +510,13 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
                 out[t] = mean[t];
                 if constexpr (MODE == kModeRsAdd) out[t] = __fadd_rn(st[0][t], mean[t]);
                 if constexpr (MODE == kModeRsAvgNorm) {
-                    out[t] = __fdiv_rn(__fadd_rn(st[0][t], mean[t]), a.k.divisor);
+                    out[t] = __fdiv_rn(__fadd_rn(st[0][t], mean[t]), a.h.k.divisor);
                 }
                 if constexpr (ModeTraits<MODE>::kNorm) {
                     if (t < nv) two_sum_add1(sq_s, sq_c, __fmul_rn(out[t], out[t]));
                 }
             }
-            float* dst = state_ptr<MODE>(a, u, 0, g.r) + j;
+            float* dst = state_ptr<MODE, A>(a, u, 0, g.r) + j;
             if (nv == kVec) {
                 st_f32x8(dst, out);
             } else {
@@ -400,16 +527,17 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
             for (int t = 0; t < kVec; ++t) {
                 float gr = mean[t];
                 if constexpr (MODE == kModeAccumFinal) {
-                    gr = __fdiv_rn(__fadd_rn(st[3][t], mean[t]), a.k.divisor);
+                    gr = __fdiv_rn(__fadd_rn(st[3][t], mean[t]), a.h.k.divisor);
                 }
                 if constexpr (MODE == kModeFromShard) {
                     gr = clip_coef == 1.0f ? st[3][t] : __fmul_rn(st[3][t], clip_coef);
                 }
-                adamw_update(a.k, gr, st[0][t], st[1][t], st[2][t]);
+                if constexpr (MODE == kModeMeanDiv) gr = __fdiv_rn(mean[t], a.h.k.divisor);
+                adamw_update(a.h.k, gr, st[0][t], st[1][t], st[2][t]);
             }
-            float* master = state_ptr<MODE>(a, u, 0, g.r) + j;
-            float* m = state_ptr<MODE>(a, u, 1, g.r) + j;
-            float* v = state_ptr<MODE>(a, u, 2, g.r) + j;
+            float* master = state_ptr<MODE, A>(a, u, 0, g.r) + j;
+            float* m = state_ptr<MODE, A>(a, u, 1, g.r) + j;
+            float* v = state_ptr<MODE, A>(a, u, 2, g.r) + j;
             if (nv == kVec) {
                 st_f32x8(master, st[0]);
                 st_f32x8(m, st[1]);
@@ -418,9 +546,25 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
                                            pack_bf16x2(st[0][2], st[0][3]),
                                            pack_bf16x2(st[0][4], st[0][5]),
                                            pack_bf16x2(st[0][6], st[0][7]));
-                const int mis = static_cast<int>(e & 7);
-                for (int o = 0; o < u->n_out; ++o) {
-                    store_bf16x8(ptr_at<uint16_t*>(a, u->off_out + o), e, mis, w);
+                if constexpr (ALIGNED) {
+                    for (int o = 0; o < u->n_out; ++o) {
+                        *reinterpret_cast<uint4*>(ptr_at<uint16_t*, A>(a, u->off_out + o) + e) = w;
+                    }
+                } else {
+                    const int mis = static_cast<int>(e & 7);
+                    // An odd offset would leave store_bf16x8 eight 2-byte stores
+                    // per lane; the warp then realigns through shuffles and
+                    // issues one aligned 16-byte store per lane.  Even offsets
+                    // keep the plain 4- or 8-byte stores (measured faster there).
+                    const bool by_warp = warp_full && (mis & 1);
+                    for (int o = 0; o < u->n_out; ++o) {
+                        uint16_t* dst = ptr_at<uint16_t*, A>(a, u->off_out + o);
+                        if (by_warp) {
+                            store_bf16x8_warp(dst, e, mis, w, lane);
+                        } else {
+                            store_bf16x8(dst, e, mis, w);
+                        }
+                    }
                 }
             } else {
                 for (int t = 0; t < nv; ++t) {
@@ -429,7 +573,7 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
                     v[t] = st[2][t];
                     const uint16_t b = float_to_bf16_rn(st[0][t]);
                     for (int o = 0; o < u->n_out; ++o) {
-                        ptr_at<uint16_t*>(a, u->off_out + o)[e + t] = b;
+                        ptr_at<uint16_t*, A>(a, u->off_out + o)[e + t] = b;
                     }
                 }
             }
@@ -447,9 +591,13 @@ __device__ void consumer_loop(const MultiArgs& a, const uint8_t* smem, uint64_t*
 
 }  // namespace
 
-template <int MODE>
+// LEAD: every unit's whole tile fits the first stage (lead_ranks).  ALIGNED:
+// every unit's shard length S is a multiple of 8, so every rank's slice and
+// every thread's 8 elements start on the 16-byte grid and no realignment code
+// is compiled in.
+template <int MODE, class A, class GT = uint16_t, bool LEAD = false, bool ALIGNED = false>
 __global__ void __launch_bounds__(kTmaThreads, 1)
-staged_step_kernel(const __grid_constant__ MultiArgs a) {
+staged_step_kernel(const __grid_constant__ A a) {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ __align__(8) uint64_t full[kStages];
     __shared__ __align__(8) uint64_t empty[kStages];
@@ -471,27 +619,30 @@ staged_step_kernel(const __grid_constant__ MultiArgs a) {
             // Total norm from the norm launches' partial sums, in a fixed order,
             // so every CTA derives the same coefficient.
             double total = 0.0;
-            for (int i = 0; i < a.n_partials; ++i) total += a.partials[i];
+            for (int i = 0; i < a.h.n_partials; ++i) total += a.h.partials[i];
             const double norm = sqrt(total);
-            const double coef = a.max_norm / (norm + 1e-6);
+            const double coef = a.h.max_norm / (norm + 1e-6);
             clip_coef = coef >= 1.0 ? 1.0f : static_cast<float>(coef);
-            if (blockIdx.x == 0 && a.norm_out != nullptr) *a.norm_out = static_cast<float>(norm);
+            if (blockIdx.x == 0 && a.h.norm_out != nullptr) *a.h.norm_out = static_cast<float>(norm);
         }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncthreads();
     if (threadIdx.x >= kConsumers) {
-        if (threadIdx.x == kConsumers) producer_loop<MODE>(a, smem, full, empty, &abort_flag, &issued);
+        if (threadIdx.x == kConsumers) {
+            producer_loop<MODE, A, GT, LEAD>(a, smem, full, empty, &abort_flag, &issued);
+        }
     } else {
-        consumer_loop<MODE>(a, smem, full, empty, &abort_flag, &consumed_min, clip_coef, warp_sq);
+        consumer_loop<MODE, A, GT, LEAD, ALIGNED>(a, smem, full, empty, &abort_flag,
+                                                  &consumed_min, clip_coef, warp_sq);
     }
     __syncthreads();
     if constexpr (ModeTraits<MODE>::kNorm) {
         if (threadIdx.x == 0) {
             double total = 0.0;
             for (int w = 0; w < kConsumerWarps; ++w) total += warp_sq[w];
-            a.partials[a.partial_base + blockIdx.x] = total;
+            a.h.partials[a.h.partial_base + blockIdx.x] = total;
         }
     }
     if (threadIdx.x == 0 && abort_flag) {
@@ -506,47 +657,112 @@ staged_step_kernel(const __grid_constant__ MultiArgs a) {
 
 constexpr size_t kStagedSmem = static_cast<size_t>(kStages) * kStageBytes;
 
-template <int MODE>
+// Raise the kernel's dynamic shared-memory limit once per device.
+template <int MODE, class A, class GT = uint16_t, bool LEAD = false, bool ALIGNED = false>
+static cudaError_t prepare_kernel(const void* kfn) {
+    static std::atomic<uint64_t> done_mask{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = dev < 64 ? (1ull << dev) : 0;
+    if (bit != 0 && (done_mask.load(std::memory_order_acquire) & bit)) return cudaSuccess;
+    e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kStagedSmem));
+    if (e == cudaSuccess && bit != 0) done_mask.fetch_or(bit, std::memory_order_release);
+    return e;
+}
+
+template <int MODE, class A>
 static int grid_for(int total_tiles) {
-    const void* kfn = reinterpret_cast<const void*>(&staged_step_kernel<MODE>);
-    cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                         static_cast<int>(kStagedSmem));
+    const void* kfn = reinterpret_cast<const void*>(&staged_step_kernel<MODE, A>);
+    prepare_kernel<MODE, A>(kfn);
     return persistent_grid(kfn, kTmaThreads, kStagedSmem, total_tiles);
 }
 
-template <int MODE>
-static cudaError_t launch_staged(const MultiArgs& a, cudaStream_t stream) {
-    const void* kfn = reinterpret_cast<const void*>(&staged_step_kernel<MODE>);
-    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(kStagedSmem));
+template <int MODE, class A, class GT, bool LEAD, bool ALIGNED>
+static cudaError_t launch_as(const A& a, cudaStream_t stream) {
+    const void* kfn =
+        reinterpret_cast<const void*>(&staged_step_kernel<MODE, A, GT, LEAD, ALIGNED>);
+    cudaError_t e = prepare_kernel<MODE, A, GT, LEAD, ALIGNED>(kfn);
     if (e != cudaSuccess) return e;
-    const int grid = persistent_grid(kfn, kTmaThreads, kStagedSmem, a.total_tiles);
-    staged_step_kernel<MODE><<<grid, kTmaThreads, kStagedSmem, stream>>>(a);
+    const int grid = persistent_grid(kfn, kTmaThreads, kStagedSmem, a.h.total_tiles);
+    staged_step_kernel<MODE, A, GT, LEAD, ALIGNED>
+        <<<grid, kTmaThreads, kStagedSmem, stream>>>(a);
     return cudaGetLastError();
 }
 
-int staged_grid(int mode, int total_tiles) {
-    switch (mode) {
-        case kModePlain: return grid_for<kModePlain>(total_tiles);
-        case kModeAccumFinal: return grid_for<kModeAccumFinal>(total_tiles);
-        case kModeRsStore: return grid_for<kModeRsStore>(total_tiles);
-        case kModeRsAdd: return grid_for<kModeRsAdd>(total_tiles);
-        case kModeRsNorm: return grid_for<kModeRsNorm>(total_tiles);
-        case kModeRsAvgNorm: return grid_for<kModeRsAvgNorm>(total_tiles);
-        default: return grid_for<kModeFromShard>(total_tiles);
-    }
+// Copy the used part of the host's full argument block into a smaller one.
+template <class A>
+static const A& shrink(const MultiArgs& big, int n_ptrs) {
+    static thread_local A small;
+    small.h = big.h;
+    for (int i = 0; i < big.h.n_units; ++i) small.unit[i] = big.unit[i];
+    for (int i = 0; i < n_ptrs; ++i) small.ptrs[i] = big.ptrs[i];
+    return small;
 }
 
-cudaError_t launch_staged_step(const MultiArgs& a, int mode, cudaStream_t stream) {
-    if (a.total_tiles <= 0) return cudaSuccess;
+// The smaller argument block when the launch fits it (a launch copies its
+// whole block), else the full one.
+template <int MODE, class GT, bool LEAD, bool ALIGNED>
+static cudaError_t launch_form(const MultiArgs& a, int n_ptrs, cudaStream_t stream) {
+    if (a.h.n_units <= MultiArgsS::kUnits && n_ptrs <= MultiArgsS::kPtrs) {
+        return launch_as<MODE, MultiArgsS, GT, LEAD, ALIGNED>(shrink<MultiArgsS>(a, n_ptrs),
+                                                              stream);
+    }
+    return launch_as<MODE, MultiArgs, GT, LEAD, ALIGNED>(a, stream);
+}
+
+// Pick the kernel form: LEAD when every unit's whole tile fits one stage, the
+// ALIGNED form of the fused step when every unit's S is a multiple of 8.
+template <int MODE, class GT = uint16_t>
+static cudaError_t launch_sized(const MultiArgs& a, int n_ptrs, cudaStream_t stream) {
+    constexpr int NS = ModeTraits<MODE>::kStateArrays;
+    constexpr bool kCanLead = can_lead<NS, GT>() && ModeTraits<MODE>::kReadsGrads;
+    constexpr bool kHasAligned =
+        sizeof(GT) == 2 && (MODE == kModePlain || MODE == kModeAccumFinal);
+    int max_ranks = 0;
+    bool aligned = true;
+    for (int i = 0; i < a.h.n_units; ++i) {
+        if (a.unit[i].n_ranks > max_ranks) max_ranks = a.unit[i].n_ranks;
+        if (a.unit[i].S % 8 != 0) aligned = false;
+    }
+    const bool lead = kCanLead && max_ranks <= first_stage_ranks<GT>(NS);
+    if constexpr (kHasAligned) {
+        if (aligned) {
+            if constexpr (kCanLead) {
+                if (lead) return launch_form<MODE, GT, true, true>(a, n_ptrs, stream);
+            }
+            return launch_form<MODE, GT, false, true>(a, n_ptrs, stream);
+        }
+    }
+    if constexpr (kCanLead) {
+        if (lead) return launch_form<MODE, GT, true, false>(a, n_ptrs, stream);
+    }
+    return launch_form<MODE, GT, false, false>(a, n_ptrs, stream);
+}
+
+cudaError_t launch_staged_step_f32(const MultiArgs& a, int n_ptrs, cudaStream_t stream) {
+    if (a.h.total_tiles <= 0) return cudaSuccess;
+    return launch_sized<kModeMeanDiv, float>(a, n_ptrs, stream);
+}
+
+int staged_grid(int mode, int total_tiles) {
+    // The grid depends only on the kernel's resources, which every block size
+    // and mode share; the smallest instantiation stands for all.
+    (void)mode;
+    return grid_for<kModePlain, MultiArgsS>(total_tiles);
+}
+
+cudaError_t launch_staged_step(const MultiArgs& a, int n_ptrs, int mode, cudaStream_t stream) {
+    if (a.h.total_tiles <= 0) return cudaSuccess;
     switch (mode) {
-        case kModePlain: return launch_staged<kModePlain>(a, stream);
-        case kModeAccumFinal: return launch_staged<kModeAccumFinal>(a, stream);
-        case kModeRsStore: return launch_staged<kModeRsStore>(a, stream);
-        case kModeRsAdd: return launch_staged<kModeRsAdd>(a, stream);
-        case kModeRsNorm: return launch_staged<kModeRsNorm>(a, stream);
-        case kModeRsAvgNorm: return launch_staged<kModeRsAvgNorm>(a, stream);
-        default: return launch_staged<kModeFromShard>(a, stream);
+        case kModePlain: return launch_sized<kModePlain>(a, n_ptrs, stream);
+        case kModeAccumFinal: return launch_sized<kModeAccumFinal>(a, n_ptrs, stream);
+        case kModeRsStore: return launch_sized<kModeRsStore>(a, n_ptrs, stream);
+        case kModeRsAdd: return launch_sized<kModeRsAdd>(a, n_ptrs, stream);
+        case kModeRsNorm: return launch_sized<kModeRsNorm>(a, n_ptrs, stream);
+        case kModeRsAvgNorm: return launch_sized<kModeRsAvgNorm>(a, n_ptrs, stream);
+        default: return launch_sized<kModeFromShard>(a, n_ptrs, stream);
     }
 }
 

@@ -34,12 +34,12 @@ class ZeroLayout(ctypes.Structure):
     """zero_layout_t: FlatParameter layout of one FSDP unit."""
     _fields_ = [("n_tensors", ctypes.c_int64), ("numel", ctypes.c_int64),
                 ("numel_padded", ctypes.c_int64), ("shard_numel", ctypes.c_int64),
-                ("n_ranks", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("n_ranks", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
     def __repr__(self):
         return (f"ZeroLayout(n_tensors={self.n_tensors}, numel={self.numel}, "
                 f"numel_padded={self.numel_padded}, shard_numel={self.shard_numel}, "
-                f"n_ranks={self.n_ranks})")
+                f"n_ranks={self.n_ranks}, flags={self.flags})")
 
 
 class ZeroUnit(ctypes.Structure):
@@ -103,6 +103,14 @@ def load() -> ctypes.CDLL:
         lib.zero_step_units_clip_noalloc.argtypes = [ctypes.POINTER(ZeroUnit), i32, i32, i32,
                                                      hp, ctypes.c_double, p, p]
         lib.zero_step_units_clip_noalloc.restype = ctypes.c_int
+        lib.zero1_accumulate.argtypes = [p, p, i32, lay, p]
+        lib.zero1_accumulate.restype = ctypes.c_int
+        lib.zero1_step.argtypes = [p, i32, p, p, p, p, i32, lay, hp, p]
+        lib.zero1_step.restype = ctypes.c_int
+        lib.zero_param_layout.argtypes = [i64, i64, i32, lay]
+        lib.zero_param_layout.restype = ctypes.c_int
+        lib.zero_shard_numel.argtypes = [lay, i32, ctypes.POINTER(ctypes.c_int64)]
+        lib.zero_shard_numel.restype = ctypes.c_int
         lib.zero_device_status.argtypes = [p, ctypes.POINTER(ctypes.c_int32), i32]
         lib.zero_device_status.restype = ctypes.c_int
         lib.zero_selftest_wait_timeout.argtypes = [i64, p]
@@ -265,6 +273,29 @@ def zero_selftest_wait_timeout(limit_ns: int, stream=None):
            "zero_selftest_wait_timeout")
 
 
+class PreparedUnits:
+    """Units marshalled once into a zero_unit_t array, for calls that step the
+    same buffers every iteration (saves rebuilding the pointer tables)."""
+
+    def __init__(self, units):
+        self.n = len(units)
+        self.array, self._keep = _unit_array(units)
+
+    def __len__(self):
+        return self.n
+
+
+def prepare_units(units) -> PreparedUnits:
+    return PreparedUnits(units)
+
+
+def _units_arg(units):
+    if isinstance(units, PreparedUnits):
+        return units.array, None, units.n
+    arr, keep = _unit_array(units)
+    return arr, keep, len(units)
+
+
 def _unit_array(units):
     """Marshal (grads, master, m, v, accum or None, full_params, layout) tuples
     into a zero_unit_t array; returns (array, keep-alive list)."""
@@ -285,18 +316,19 @@ def _unit_array(units):
 
 
 def zero_step_units(units, micro_step: int, n_micro: int, hp, stream=None):
-    """units: sequence of (grads, master, m, v, accum or None, full_params, layout)."""
-    arr, keep = _unit_array(units)
+    """units: sequence of (grads, master, m, v, accum or None, full_params,
+    layout), or a PreparedUnits."""
+    arr, keep, n = _units_arg(units)
     h = _hp(hp)
-    _check(load().zero_step_units(arr, len(units), int(micro_step), int(n_micro),
+    _check(load().zero_step_units(arr, n, int(micro_step), int(n_micro),
                                   ctypes.byref(h) if h is not None else None, _stream(stream)),
            "zero_step_units")
 
 
 def zero_clip_workspace_bytes(units, n_micro: int = 1) -> int:
-    arr, keep = _unit_array(units)
+    arr, keep, n = _units_arg(units)
     out = ctypes.c_int64(0)
-    _check(load().zero_clip_workspace_bytes(arr, len(units), int(n_micro), ctypes.byref(out)),
+    _check(load().zero_clip_workspace_bytes(arr, n, int(n_micro), ctypes.byref(out)),
            "zero_clip_workspace_bytes")
     return int(out.value)
 
@@ -306,9 +338,9 @@ def zero_step_units_clip(units, micro_step: int, n_micro: int, hp, max_norm: flo
     """zero_step_units with global gradient-norm clipping; every unit needs an
     accumulator (it receives the averaged gradient).  workspace: device
     buffer of at least zero_clip_workspace_bytes(units, n_micro) bytes."""
-    arr, keep = _unit_array(units)
+    arr, keep, n = _units_arg(units)
     h = _hp(hp)
-    _check(load().zero_step_units_clip(arr, len(units), int(micro_step), int(n_micro),
+    _check(load().zero_step_units_clip(arr, n, int(micro_step), int(n_micro),
                                        ctypes.byref(h) if h is not None else None,
                                        float(max_norm), _addr(workspace) or None,
                                        int(workspace_bytes), _addr(norm_out) or None,
@@ -324,9 +356,43 @@ def zero_step_units_clip_noalloc(units, micro_step: int, n_micro: int, hp, max_n
     allocate device memory: the partial sums live in a fixed 32 KB scratch
     array inside the library, shared by every call (serialise calls that could
     overlap on the GPU)."""
-    arr, keep = _unit_array(units)
+    arr, keep, n = _units_arg(units)
     h = _hp(hp)
-    _check(load().zero_step_units_clip_noalloc(arr, len(units), int(micro_step), int(n_micro),
+    _check(load().zero_step_units_clip_noalloc(arr, n, int(micro_step), int(n_micro),
                                                ctypes.byref(h) if h is not None else None,
                                                float(max_norm), _addr(norm_out) or None,
                                                _stream(stream)), "zero_step_units_clip_noalloc")
+
+
+def zero1_accumulate(grads, full_accum, first: bool, layout: ZeroLayout, stream=None):
+    """ZeRO-1 local accumulation: full_accum[k] = (first ? 0 : full_accum[k]) + grads[k]."""
+    _check(load().zero1_accumulate(_ptrs(grads), _ptrs(full_accum), int(bool(first)),
+                                   ctypes.byref(layout), _stream(stream)), "zero1_accumulate")
+
+
+def zero1_step(full_accum, n_micro: int, master, m, v, full_params, layout: ZeroLayout, hp,
+               stream=None):
+    """ZeRO-1 step: one reduce-scatter of the accumulated fp32 gradients / n_micro,
+    then AdamW, bf16 cast and all-gather."""
+    h = _hp(hp)
+    _check(load().zero1_step(_ptrs(full_accum), int(n_micro), _ptrs(master), _ptrs(m), _ptrs(v),
+                             _ptrs(full_params), len(full_params), ctypes.byref(layout),
+                             ctypes.byref(h), _stream(stream)), "zero1_step")
+
+
+ZERO_LAYOUT_UNPADDED = 1
+
+
+def zero_param_layout(dim0: int, row_numel: int, n_ranks: int) -> ZeroLayout:
+    """FSDP2 per-parameter Shard(0) layout of one parameter (no padding)."""
+    layout = ZeroLayout()
+    _check(load().zero_param_layout(int(dim0), int(row_numel), int(n_ranks),
+                                    ctypes.byref(layout)), "zero_param_layout")
+    return layout
+
+
+def zero_shard_numel(layout: ZeroLayout, rank: int) -> int:
+    out = ctypes.c_int64(0)
+    _check(load().zero_shard_numel(ctypes.byref(layout), int(rank), ctypes.byref(out)),
+           "zero_shard_numel")
+    return int(out.value)

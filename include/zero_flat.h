@@ -60,15 +60,21 @@ enum {
     ZERO_ERR_CUDA = -4         /* the CUDA runtime reported an error at launch        */
 };
 
-/* FlatParameter layout of one FSDP unit ([L5] section 7.1; [LA] section 5.1). */
+/* FlatParameter layout of one FSDP unit ([L5] section 7.1; [LA] section 5.1),
+ * or (flags = ZERO_LAYOUT_UNPADDED, from zero_param_layout) the per-parameter
+ * Shard(0) layout of one parameter. */
 typedef struct zero_layout {
     int64_t n_tensors;    /* tensors flattened into the unit                   */
     int64_t numel;        /* P: sum of the tensors' element counts             */
     int64_t numel_padded; /* P_pad: P rounded up to a multiple of n_ranks      */
     int64_t shard_numel;  /* S = P_pad / n_ranks; rank r owns [r*S, (r+1)*S)   */
     int32_t n_ranks;      /* N_d logical data-parallel ranks                   */
-    int32_t reserved;     /* zero                                               */
+    int32_t flags;        /* 0, or ZERO_LAYOUT_UNPADDED                        */
 } zero_layout_t;
+
+/* No padding exists in memory: gradient and parameter buffers hold numel
+ * elements and rank r's state shard holds clamp(numel - r*S, 0, S). */
+#define ZERO_LAYOUT_UNPADDED 1
 
 /* AdamW hyper-parameters of one optimizer step ([DZ] section 4.2).  Doubles:
  * the library derives its fp32 kernel constants (bias corrections included)
@@ -95,6 +101,25 @@ typedef struct zero_adamw {
  */
 int zero_flat_layout(const int64_t* numels, int64_t n_tensors, int32_t n_ranks,
                      int64_t* offsets_out, zero_layout_t* layout_out);
+
+/*
+ * zero_param_layout -- host only.  FSDP2 per-parameter Shard(0) ([L5] section
+ * 7.2: every parameter keeps its shape and is split along dim 0 over the
+ * ranks, with no FlatParameter and no padding; [A03] section 4; [LA] section
+ * 9.5).  A parameter of dim0 rows of row_numel elements is cut the way a tensor
+ * is chunked into n_ranks pieces: S = ceil(dim0 / n_ranks) * row_numel, rank r
+ * owns elements [r*S, min((r+1)*S, numel)) -- possibly none.  The layout has
+ * flags = ZERO_LAYOUT_UNPADDED and numel_padded = n_ranks * S (a virtual size:
+ * nothing of it beyond numel is allocated or touched).  Such layouts are
+ * accepted by zero_step, zero_step_units(_clip) and zero_reduce_scatter (the
+ * staged kernels); the other device entry points reject them.
+ * Errors: ZERO_ERR_INVALID_ARG (non-positive sizes), ZERO_ERR_SIZE (overflow).
+ */
+int zero_param_layout(int64_t dim0, int64_t row_numel, int32_t n_ranks, zero_layout_t* layout_out);
+
+/* Elements of rank `rank`'s shard under `layout` (S, fewer, or 0 at the end
+ * of an unpadded layout). */
+int zero_shard_numel(const zero_layout_t* layout, int32_t rank, int64_t* numel_out);
 
 /*
  * zero_shard_segments -- host only.  ([LA] section 5.1: a rank's slice cuts
@@ -319,6 +344,31 @@ int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t
 int zero_step_units_clip_noalloc(const zero_unit_t* units, int32_t n_units, int32_t micro_step,
                                  int32_t n_micro, const zero_adamw_t* hp, double max_norm,
                                  float* norm_out, void* stream);
+
+/*
+ * zero1_accumulate / zero1_step -- device.  The ZeRO-1 form of gradient
+ * accumulation ([L5] section 3: with ZeRO-1 each rank still holds its full
+ * gradient, so it can accumulate the micro-batches locally and reduce-scatter
+ * once, at the last one; ZeRO-2 keeps only its shard and must reduce-scatter
+ * every micro-batch, which is what zero_step's accumulator does; [L5]
+ * section 2: the fp32 accumulator costs +4 Psi per rank under ZeRO-1 and
+ * +4 Psi / N_d under ZeRO-2).
+ *   zero1_accumulate: for every rank k and e < P_pad,
+ *     full_accum[k][e] = (first ? 0 : full_accum[k][e]) + grads[k][e]   (fp32)
+ *     grads[n_ranks]       bf16, each P_pad;   full_accum[n_ranks] fp32, each P_pad
+ *   zero1_step: after n_micro micro-steps, the single reduce-scatter of the
+ *     accumulators by averaging (compensated fp32 sum in rank order), divided
+ *     by n_micro, then AdamW, bf16 cast and all-gather exactly as zero_step.
+ * Per element and micro-step zero1_accumulate moves 6 (first) or 10 bytes per
+ * rank and zero1_step 4*N_d + 26, against 2*N_d + 4..8 and 2*N_d + 30 for the
+ * ZeRO-2 form: with every rank in one GPU the communication ZeRO-1 saves is
+ * free and its local accumulation costs HBM traffic instead.
+ */
+int zero1_accumulate(const uint16_t* const* grads, float* const* full_accum, int32_t first,
+                     const zero_layout_t* layout, void* stream);
+int zero1_step(const float* const* full_accum, int32_t n_micro, float* const* master,
+               float* const* m, float* const* v, uint16_t* const* full_params, int32_t n_out,
+               const zero_layout_t* layout, const zero_adamw_t* hp, void* stream);
 
 /* Message for the last non-OK return on the calling thread ("" if none). */
 const char* zero_last_error(void);

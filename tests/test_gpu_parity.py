@@ -51,6 +51,11 @@ CASES = [
     ("gather_to_every_rank", [10007], 4, 4, 1, 2),
     ("accumulate_4_micro_steps", [100003], 8, 1, 4, 2),
     ("accumulate_3_micro_steps", [40001], 5, 2, 3, 2),
+    # every shard a multiple of 8 elements: the kernels' aligned forms
+    ("aligned_two_ranks", [2 * 8 * 5000], 2, 1, 1, 3),
+    ("aligned_one_rank_two_outputs", [8 * 1111, 8 * 7], 1, 2, 1, 2),
+    ("aligned_eight_ranks_two_outputs", [8 * 8 * 3001], 8, 2, 1, 2),
+    ("aligned_accumulate_3_micro_steps", [16 * 8 * 777], 16, 1, 3, 2),
 ]
 
 
@@ -77,7 +82,9 @@ def test_small_cases(oracle, kernel, name, numels, n_ranks, n_out, n_micro, step
 
 @pytest.mark.parametrize("numels,n_ranks,n_micro", [([4096 * 1024, 1024, 1000], 4, 1),
                                                     ([999999], 3, 1), ([64 * 4099 + 5], 64, 2),
-                                                    ([77777], 65, 3), ([5], 8, 1)])
+                                                    ([77777], 65, 3), ([5], 8, 1),
+                                                    ([2 * 8 * 70001], 2, 1),
+                                                    ([8 * 8 * 1234], 8, 2)])
 def test_staged_equals_direct_bitwise(monkeypatch, numels, n_ranks, n_micro):
     """The bulk-copy staged kernels and the direct-load kernels give identical bits."""
     units = {}
@@ -306,3 +313,23 @@ def test_step_units_against_oracle(oracle):
                                           weight_decay=hp["weight_decay"], step=t)
     for c in cases:
         c.compare()
+
+
+def test_prepared_units_same_as_list():
+    """Units marshalled once (prepare_units) step exactly like a fresh list."""
+    specs = [([768, 9000], 8), ([50000, 5], 8), ([64 * 33 + 1], 64)]
+    a_units, b_units = _units(specs, tag="pu"), _units(specs, tag="pu")
+    prepared = zf.zero.prepare_units([_unit_tuple(a, False) for a in a_units])
+    for t in (1, 2, 3):
+        for i, (a, b) in enumerate(zip(a_units, b_units)):
+            g = synthetic.make_grads(a.P, a.n_ranks, 1e-2, ("pu", i, t)).cuda()
+            a.grads.copy_(g)
+            b.grads.copy_(g)
+        zf.zero_step_units(prepared, 1, 1, hp_at(t))
+        zf.zero_step_units([_unit_tuple(b, False) for b in b_units], 1, 1, hp_at(t))
+    torch.cuda.synchronize()
+    for a, b in zip(a_units, b_units):
+        assert torch.equal(a.master.contiguous().view(torch.int32),
+                           b.master.contiguous().view(torch.int32))
+        assert torch.equal(a.params.contiguous().view(torch.int16),
+                           b.params.contiguous().view(torch.int16))
