@@ -259,4 +259,30 @@ __device__ __forceinline__ void adamw_update(const AdamConsts& k, float g, float
     v = v_new;
 }
 
+// Two elements at once: the operations of adamw_update, lane by lane, on
+// packed fp32 pairs.  FFMA2 / FMUL2 round each lane exactly as the scalar
+// instructions do, so the results are bit-identical to two adamw_update calls
+// in fewer instructions (square root and division stay scalar).
+__device__ __forceinline__ float2 splat2(float x) { return make_float2(x, x); }
+
+__device__ __forceinline__ void adamw_update2(const AdamConsts& k, float2 g, float2& theta,
+                                              float2& m, float2& v) {
+    const float2 corr_m =
+        __ffma2_rn(splat2(k.beta1_lo), m, __fmul2_rn(splat2(k.one_minus_beta1_lo), g));
+    const float2 m_new = __ffma2_rn(splat2(k.beta1), m,
+                                    __ffma2_rn(splat2(k.one_minus_beta1), g, corr_m));
+    const float2 gg = __fmul2_rn(g, g);
+    const float2 corr_v =
+        __ffma2_rn(splat2(k.beta2_lo), v, __fmul2_rn(splat2(k.one_minus_beta2_lo), gg));
+    const float2 v_new = __ffma2_rn(splat2(k.beta2), v,
+                                    __ffma2_rn(splat2(k.one_minus_beta2), gg, corr_v));
+    const float2 root = make_float2(__fsqrt_rn(v_new.x), __fsqrt_rn(v_new.y));
+    const float2 denom = __ffma2_rn(root, splat2(k.inv_sqrt_bc2), splat2(k.eps));
+    const float2 upd = make_float2(__fdiv_rn(m_new.x, denom.x), __fdiv_rn(m_new.y, denom.y));
+    const float2 decayed = __ffma2_rn(splat2(-k.lr_wd), theta, theta);
+    theta = __ffma2_rn(splat2(-k.step_size), upd, decayed);
+    m = m_new;
+    v = v_new;
+}
+
 }  // namespace zf

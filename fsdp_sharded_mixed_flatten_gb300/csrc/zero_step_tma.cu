@@ -33,6 +33,7 @@
 // of the CTA to stop, and the CTA waits (bounded again) for the copies it
 // issued before it returns.
 #include <atomic>
+#include <type_traits>
 
 #include "zero_kernels.cuh"
 
@@ -280,13 +281,13 @@ __device__ __forceinline__ float* state_ptr(const A& a, const UnitDesc* u, int a
 // thread's 8 elements starting A elements into its aligned pair of words.
 // fp32 gradient slices: a thread's 8 values start A words into its three
 // aligned 16-byte words.
-template <int A>
+template <int A, int RMAX>
 __device__ __forceinline__ void consume_stage_f32(const uint8_t* stage, int nk, int tid,
                                                   float2 (&s)[4], float2 (&c)[4]) {
     constexpr int kSlice = slice_bytes<float>();
     const uint8_t* base = stage + tid * 32;
 #pragma unroll
-    for (int kk = 0; kk < GradTraits<float>::kRanksPerStage; ++kk) {
+    for (int kk = 0; kk < RMAX; ++kk) {
         if (kk < nk) {
             const float4* p = reinterpret_cast<const float4*>(base + kk * kSlice);
             const float4 x0 = p[0], x1 = p[1];
@@ -301,12 +302,12 @@ __device__ __forceinline__ void consume_stage_f32(const uint8_t* stage, int nk, 
     }
 }
 
-template <int A>
+template <int A, int RMAX>
 __device__ __forceinline__ void consume_stage(const uint8_t* stage, int nk, int tid,
                                               float2 (&s)[4], float2 (&c)[4]) {
     const uint8_t* base = stage + tid * 16;
 #pragma unroll
-    for (int kk = 0; kk < GradTraits<uint16_t>::kRanksPerStage; ++kk) {
+    for (int kk = 0; kk < RMAX; ++kk) {
         if (kk < nk) {
             const uint4* p = reinterpret_cast<const uint4*>(base + kk * kSliceBytes);
             uint4 x = p[0];
@@ -397,27 +398,30 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
         const bool vec = (nv == kVec) && (e + kVec <= g.a1);
         const int n_gr = ModeTraits<MODE>::kReadsGrads ? n_ranks : 0;
         // Ranks [k0, k0 + nk) of the tile from one stage into (s, c).
-        auto consume = [&](const uint8_t* stage, int k0, int nk) {
+        // (rmax: a compile-time bound on nk, so that a LEAD launch's first
+        // stage unrolls only the ranks it can hold)
+        auto consume = [&](const uint8_t* stage, int k0, int nk, auto rmax) {
+            constexpr int RM = decltype(rmax)::value;
             if (vec) {
                 if constexpr (ALIGNED) {
-                    consume_stage<0>(stage, nk, tid, s, c);
+                    consume_stage<0, RM>(stage, nk, tid, s, c);
                 } else if constexpr (sizeof(GT) == 4) {
                     switch (g.mis) {
-                        case 0: consume_stage_f32<0>(stage, nk, tid, s, c); break;
-                        case 1: consume_stage_f32<1>(stage, nk, tid, s, c); break;
-                        case 2: consume_stage_f32<2>(stage, nk, tid, s, c); break;
-                        default: consume_stage_f32<3>(stage, nk, tid, s, c); break;
+                        case 0: consume_stage_f32<0, RM>(stage, nk, tid, s, c); break;
+                        case 1: consume_stage_f32<1, RM>(stage, nk, tid, s, c); break;
+                        case 2: consume_stage_f32<2, RM>(stage, nk, tid, s, c); break;
+                        default: consume_stage_f32<3, RM>(stage, nk, tid, s, c); break;
                     }
                 } else {
                     switch (g.mis) {
-                        case 0: consume_stage<0>(stage, nk, tid, s, c); break;
-                        case 1: consume_stage<1>(stage, nk, tid, s, c); break;
-                        case 2: consume_stage<2>(stage, nk, tid, s, c); break;
-                        case 3: consume_stage<3>(stage, nk, tid, s, c); break;
-                        case 4: consume_stage<4>(stage, nk, tid, s, c); break;
-                        case 5: consume_stage<5>(stage, nk, tid, s, c); break;
-                        case 6: consume_stage<6>(stage, nk, tid, s, c); break;
-                        default: consume_stage<7>(stage, nk, tid, s, c); break;
+                        case 0: consume_stage<0, RM>(stage, nk, tid, s, c); break;
+                        case 1: consume_stage<1, RM>(stage, nk, tid, s, c); break;
+                        case 2: consume_stage<2, RM>(stage, nk, tid, s, c); break;
+                        case 3: consume_stage<3, RM>(stage, nk, tid, s, c); break;
+                        case 4: consume_stage<4, RM>(stage, nk, tid, s, c); break;
+                        case 5: consume_stage<5, RM>(stage, nk, tid, s, c); break;
+                        case 6: consume_stage<6, RM>(stage, nk, tid, s, c); break;
+                        default: consume_stage<7, RM>(stage, nk, tid, s, c); break;
                     }
                 }
             } else if (nv > 0) {
@@ -464,9 +468,14 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
 #pragma unroll
             for (int arr = 0; arr < NS; ++arr) {
                 if (from_smem) {
+                    // A thread's 32 bytes are two 16-byte words; threads 4-7 of
+                    // every 8 read their upper word first, so that each
+                    // quarter-warp's 16-byte reads fall in distinct banks.
                     const float4* p =
                         reinterpret_cast<const float4*>(stage + arr * kStateArrayBytes + first * 4);
-                    const float4 x0 = p[0], x1 = p[1];
+                    const int sw = (tid >> 2) & 1;
+                    const float4 ya = p[sw], yb = p[sw ^ 1];
+                    const float4 x0 = sw ? yb : ya, x1 = sw ? ya : yb;
                     st[arr][0] = x0.x; st[arr][1] = x0.y; st[arr][2] = x0.z; st[arr][3] = x0.w;
                     st[arr][4] = x1.x; st[arr][5] = x1.y; st[arr][6] = x1.z; st[arr][7] = x1.w;
                 } else {
@@ -476,7 +485,11 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                 }
             }
             if constexpr (NS == 0 || LEAD) {
-                if (r0 > 0) consume(stage + NS * kStateArrayBytes, 0, r0);
+                constexpr int kFirstMax = NS == 0 ? RG : first_stage_ranks<GT>(NS);
+                if (r0 > 0) {
+                    consume(stage + NS * kStateArrayBytes, 0, r0,
+                            std::integral_constant<int, kFirstMax>());
+                }
             }
             release();
         }
@@ -488,7 +501,7 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                     ok = false;
                     break;
                 }
-                consume(stage, k0, min(RG, n_gr - k0));
+                consume(stage, k0, min(RG, n_gr - k0), std::integral_constant<int, RG>());
                 release();
             }
         }
@@ -497,10 +510,20 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
         if (!ok || (nv == 0 && !warp_full)) continue;
 
         float mean[8];
+        if (u->n_pow2) {
+            // exact scaling, both lanes of a pair in one packed add and multiply
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            mean[2 * q] = finish_mean(s[q].x, c[q].x, u->n_ranks_f, u->inv_n, u->n_pow2);
-            mean[2 * q + 1] = finish_mean(s[q].y, c[q].y, u->n_ranks_f, u->inv_n, u->n_pow2);
+            for (int q = 0; q < 4; ++q) {
+                const float2 r = __fmul2_rn(__fadd2_rn(s[q], c[q]), splat2(u->inv_n));
+                mean[2 * q] = r.x;
+                mean[2 * q + 1] = r.y;
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                mean[2 * q] = finish_mean(s[q].x, c[q].x, u->n_ranks_f, u->inv_n, false);
+                mean[2 * q + 1] = finish_mean(s[q].y, c[q].y, u->n_ranks_f, u->inv_n, false);
+            }
         }
 
         if constexpr (ModeTraits<MODE>::kReduceScatter) {
@@ -523,17 +546,27 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                 for (int t = 0; t < nv; ++t) dst[t] = out[t];
             }
         } else {
+            float gr[kVec];
 #pragma unroll
             for (int t = 0; t < kVec; ++t) {
-                float gr = mean[t];
+                gr[t] = mean[t];
                 if constexpr (MODE == kModeAccumFinal) {
-                    gr = __fdiv_rn(__fadd_rn(st[3][t], mean[t]), a.h.k.divisor);
+                    gr[t] = __fdiv_rn(__fadd_rn(st[3][t], mean[t]), a.h.k.divisor);
                 }
                 if constexpr (MODE == kModeFromShard) {
-                    gr = clip_coef == 1.0f ? st[3][t] : __fmul_rn(st[3][t], clip_coef);
+                    gr[t] = clip_coef == 1.0f ? st[3][t] : __fmul_rn(st[3][t], clip_coef);
                 }
-                if constexpr (MODE == kModeMeanDiv) gr = __fdiv_rn(mean[t], a.h.k.divisor);
-                adamw_update(a.h.k, gr, st[0][t], st[1][t], st[2][t]);
+                if constexpr (MODE == kModeMeanDiv) gr[t] = __fdiv_rn(mean[t], a.h.k.divisor);
+            }
+#pragma unroll
+            for (int t = 0; t < kVec; t += 2) {
+                float2 th = make_float2(st[0][t], st[0][t + 1]);
+                float2 mm = make_float2(st[1][t], st[1][t + 1]);
+                float2 vv = make_float2(st[2][t], st[2][t + 1]);
+                adamw_update2(a.h.k, make_float2(gr[t], gr[t + 1]), th, mm, vv);
+                st[0][t] = th.x; st[0][t + 1] = th.y;
+                st[1][t] = mm.x; st[1][t + 1] = mm.y;
+                st[2][t] = vv.x; st[2][t + 1] = vv.y;
             }
             float* master = state_ptr<MODE, A>(a, u, 0, g.r) + j;
             float* m = state_ptr<MODE, A>(a, u, 1, g.r) + j;
