@@ -310,56 +310,61 @@ def time_resident(res, steps, warmup, ws, device, per_kernel=True, clocks=None):
 
 
 def time_e2e(res, steps, warmup, ws, device):
-    """Same step through the public API with host buffers: each step copies
-    every unit's gradients from pinned host memory and reads the gathered
-    bf16 parameters back."""
+    """The same step through the host-buffer entry point
+    (zero_step_units_host): every step copies every unit's gradients from
+    pinned host memory (one 2D copy per unit) and the gathered bf16 parameters
+    back.  Two device gradient sets alternate, so a step's copies overlap the
+    previous step's update; the copies of a set wait for the step that last
+    read it."""
     import torch
-    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    from fsdp_sharded_mixed_flatten_gb300 import (ZERO_HOST_GRADS_FREE, HostTables, synthetic,
+                                                  zero_step_units_host)
+    from fsdp_sharded_mixed_flatten_gb300.buffers import aligned_rows
+    from fsdp_sharded_mixed_flatten_gb300.zero import prepare_units
     hp = dict(synthetic.ADAMW_DEFAULTS)
-    host_g = [fu.grads.cpu().pin_memory() for fu in res.units]
-    host_p = [torch.empty(fu.params.shape, dtype=torch.bfloat16).pin_memory() for fu in res.units]
-    h2d = sum(x.numel() * 2 for x in host_g)
+    host_g = [fu.grads.cpu().pin_memory() for fu in res.units]          # (N_d, P_pad) each
+    host_p = [torch.empty(fu.P_pad, dtype=torch.bfloat16).pin_memory() for fu in res.units]
+    h2d = sum(x.numel() * 2 for x in host_g) * res.n_micro
     d2h = sum(x.numel() * 2 for x in host_p)
-    from fsdp_sharded_mixed_flatten_gb300 import zero_step_units
+    tables = HostTables([[hg[k] for k in range(hg.shape[0])] for hg in host_g], host_p)
+    spare = [aligned_rows(fu.n_ranks, fu.P_pad, torch.bfloat16, device, 0) for fu in res.units]
+    sets = [prepare_units([([g[k] for k in range(fu.n_ranks)], *fu.state_rows(),
+                            fu.accum_rows(), fu.param_rows(), fu.layout)
+                           for fu, g in zip(res.units, grads)])
+            for grads in ([fu.grads for fu in res.units], spare)]
+    comp = torch.cuda.current_stream()
+    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    done = {}
 
-    # The host->device copies are spread over several streams (one per copy
-    # engine) by gradient row; the step waits for all of them.
-    cur = torch.cuda.current_stream()
-    copy_streams = [torch.cuda.Stream() for _ in range(4)]
-    rows_h2d = [(fu.grads[r], hg[r]) for fu, hg in zip(res.units, host_g)
-                for r in range(fu.grads.shape[0])]
-
-    def one(step):
-        ready = cur.record_event()          # the previous step has finished reading grads
-        for s in copy_streams:
-            s.wait_event(ready)
-        for i, (dst, src) in enumerate(rows_h2d):
-            with torch.cuda.stream(copy_streams[i % len(copy_streams)]):
-                dst.copy_(src, non_blocking=True)
-        for s in copy_streams:
-            cur.wait_stream(s)
-        zero_step_units(res.prepared, 1, 1, dict(hp, step=step))
-        for fu, hpar in zip(res.units, host_p):
-            hpar.copy_(fu.params, non_blocking=True)
+    def one(i, step):
+        if i - 2 in done:
+            s_h2d.wait_event(done.pop(i - 2))    # the last step that read this set is done
+        for k in range(1, res.n_micro + 1):
+            zero_step_units_host(sets[i % 2], tables, k, res.n_micro, dict(hp, step=step),
+                                 ZERO_HOST_GRADS_FREE, s_h2d, comp, s_d2h)
+        done[i] = comp.record_event()
 
     t = 1000
-    for _ in range(warmup):
+    for i in range(warmup):
         t += 1
-        one(t)
+        one(i, t)
     torch.cuda.synchronize()
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier(ws)
     torch.cuda.nvtx.range_push("timed_e2e")
-    start.record()
-    for _ in range(steps):
+    start.record(comp)
+    s_h2d.wait_stream(comp)
+    for i in range(warmup, warmup + steps):
         t += 1
-        one(t)
-    stop.record()
+        one(i, t)
+    comp.wait_stream(s_h2d)
+    comp.wait_stream(s_d2h)
+    stop.record(comp)
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     barrier(ws)
     el = max_over_ranks(start.elapsed_time(stop) / 1e3, ws, device)
-    del host_g, host_p
+    del host_g, host_p, spare, sets
     return el, h2d, d2h
 
 

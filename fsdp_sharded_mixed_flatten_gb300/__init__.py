@@ -11,7 +11,8 @@ from .zero import (ZERO_MAX_RANKS, zero1_accumulate, zero1_step, zero_param_layo
                    zero_adamw_shard_step, zero_all_gather, zero_device_status, zero_flat_layout,
                    zero_flatten, zero_last_error, zero_reduce_scatter, zero_selftest_wait_timeout,
                    zero_shard_segments, zero_step, zero_step_units, zero_step_units_clip,
-                   zero_step_units_clip_noalloc, zero_clip_workspace_bytes, zero_unflatten)
+                   zero_step_units_clip_noalloc, zero_clip_workspace_bytes, zero_unflatten,
+                   zero_step_units_host, HostTables, ZERO_HOST_GRADS_FREE)
 
 __all__ = [
     "ZERO_MAX_RANKS", "zero1_accumulate", "zero1_step", "zero_param_layout", "zero_shard_numel", "ZeroAdamW", "ZeroError", "ZeroLayout", "load", "zero_abi_version",
@@ -20,5 +21,5 @@ __all__ = [
     "zero_last_error", "zero_reduce_scatter", "zero_selftest_wait_timeout",
     "zero_shard_segments", "zero_step", "zero_step_units", "zero_step_units_clip",
     "zero_clip_workspace_bytes", "zero_step_units_clip_noalloc",
-    "zero_unflatten",
+    "zero_unflatten", "zero_step_units_host", "HostTables", "ZERO_HOST_GRADS_FREE",
 ]

@@ -649,6 +649,113 @@ ZERO_API int zero_step_units(const zero_unit_t* units, int32_t n_units, int32_t 
                      static_cast<cudaStream_t>(stream));
 }
 
+namespace {
+
+// An event recorded on `from` that `to` waits for; released at once (the
+// wait keeps what it needs).
+int order_streams(cudaStream_t from, cudaStream_t to, const char* what) {
+    cudaEvent_t ev = nullptr;
+    cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
+    if (e == cudaSuccess) e = cudaEventRecord(ev, from);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(to, ev, 0);
+    if (ev != nullptr) {
+        const cudaError_t d = cudaEventDestroy(ev);
+        if (e == cudaSuccess) e = d;
+    }
+    return cuda_status(e, what);
+}
+
+// Rows r = 0..n-1 at base + r * pitch (pitch in bytes, at least `width`)?
+template <class T>
+bool evenly_spaced(const T* const* rows, int n, int64_t width, int64_t* pitch) {
+    if (n < 2) {
+        *pitch = width;
+        return true;
+    }
+    const auto b0 = reinterpret_cast<uintptr_t>(rows[0]);
+    const auto b1 = reinterpret_cast<uintptr_t>(rows[1]);
+    if (b1 <= b0) return false;
+    const uintptr_t p = b1 - b0;
+    if (p < static_cast<uintptr_t>(width) ||
+        p > static_cast<uintptr_t>(std::numeric_limits<int32_t>::max()))
+        return false;
+    for (int r = 2; r < n; ++r) {
+        if (reinterpret_cast<uintptr_t>(rows[r]) != b0 + p * static_cast<uintptr_t>(r)) return false;
+    }
+    *pitch = static_cast<int64_t>(p);
+    return true;
+}
+
+}  // namespace
+
+ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
+                                  const uint16_t* const* const* host_grads,
+                                  uint16_t* const* host_params, int32_t micro_step,
+                                  int32_t n_micro, const zero_adamw_t* hp, int32_t flags,
+                                  void* h2d_stream, void* compute_stream, void* d2h_stream) {
+    if (units == nullptr || n_units < 1) return fail(ZERO_ERR_INVALID_ARG, "no units");
+    if (n_units > 4096) return fail(ZERO_ERR_SIZE, "at most 4096 units per call");
+    if (host_grads == nullptr) return fail(ZERO_ERR_INVALID_ARG, "host_grads is NULL");
+    if ((flags & ~ZERO_HOST_GRADS_FREE) != 0) return fail(ZERO_ERR_INVALID_ARG, "unknown flags");
+    for (int i = 0; i < n_units; ++i) {
+        const zero_unit_t& x = units[i];
+        if (x.layout == nullptr || x.grads == nullptr || host_grads[i] == nullptr)
+            return fail(ZERO_ERR_INVALID_ARG, "unit %d: NULL layout or gradient rows", i);
+        if (int rc = check_layout(x.layout)) return rc;
+        for (int k = 0; k < x.layout->n_ranks; ++k) {
+            if (host_grads[i][k] == nullptr || x.grads[k] == nullptr)
+                return fail(ZERO_ERR_INVALID_ARG, "unit %d rank %d: NULL gradient buffer", i, k);
+        }
+    }
+    const auto h2d = static_cast<cudaStream_t>(h2d_stream);
+    const auto comp = static_cast<cudaStream_t>(compute_stream);
+    const auto d2h = static_cast<cudaStream_t>(d2h_stream);
+    if (!(flags & ZERO_HOST_GRADS_FREE)) {
+        if (int rc = order_streams(comp, h2d, "ordering the gradient copies")) return rc;
+    }
+    for (int i = 0; i < n_units; ++i) {
+        const zero_unit_t& x = units[i];
+        const int n = x.layout->n_ranks;
+        const int64_t count = unpadded(x.layout) ? x.layout->numel : x.layout->numel_padded;
+        const int64_t width = count * static_cast<int64_t>(sizeof(uint16_t));
+        int64_t dpitch = 0, spitch = 0;
+        cudaError_t e = cudaSuccess;
+        if (evenly_spaced(x.grads, n, width, &dpitch) &&
+            evenly_spaced(host_grads[i], n, width, &spitch)) {
+            e = n == 1 ? cudaMemcpyAsync(const_cast<uint16_t*>(x.grads[0]), host_grads[i][0],
+                                         static_cast<size_t>(width), cudaMemcpyHostToDevice, h2d)
+                       : cudaMemcpy2DAsync(const_cast<uint16_t*>(x.grads[0]),
+                                           static_cast<size_t>(dpitch), host_grads[i][0],
+                                           static_cast<size_t>(spitch), static_cast<size_t>(width),
+                                           static_cast<size_t>(n), cudaMemcpyHostToDevice, h2d);
+        } else {
+            for (int k = 0; k < n && e == cudaSuccess; ++k) {
+                e = cudaMemcpyAsync(const_cast<uint16_t*>(x.grads[k]), host_grads[i][k],
+                                    static_cast<size_t>(width), cudaMemcpyHostToDevice, h2d);
+            }
+        }
+        if (int rc = cuda_status(e, "gradient copy to the device")) return rc;
+    }
+    if (int rc = order_streams(h2d, comp, "ordering the step after the copies")) return rc;
+    if (int rc = zero_step_units(units, n_units, micro_step, n_micro, hp, compute_stream)) return rc;
+    const bool optimizer_runs = units[0].accum == nullptr || n_micro <= 1 || micro_step == n_micro;
+    if (host_params != nullptr && optimizer_runs) {
+        if (int rc = order_streams(comp, d2h, "ordering the parameter copies")) return rc;
+        for (int i = 0; i < n_units; ++i) {
+            const zero_unit_t& x = units[i];
+            if (host_params[i] == nullptr || x.n_out < 1 || x.full_params == nullptr) continue;
+            const int64_t count = unpadded(x.layout) ? x.layout->numel : x.layout->numel_padded;
+            if (int rc = cuda_status(
+                    cudaMemcpyAsync(host_params[i], x.full_params[0],
+                                    static_cast<size_t>(count) * sizeof(uint16_t),
+                                    cudaMemcpyDeviceToHost, d2h),
+                    "parameter copy to the host"))
+                return rc;
+        }
+    }
+    return ok();
+}
+
 ZERO_API int zero_device_status(void* stream, int32_t* status, int32_t clear) {
     if (status == nullptr) return fail(ZERO_ERR_INVALID_ARG, "status is NULL");
     int v = 0;

@@ -103,6 +103,9 @@ def load() -> ctypes.CDLL:
         lib.zero_step_units_clip_noalloc.argtypes = [ctypes.POINTER(ZeroUnit), i32, i32, i32,
                                                      hp, ctypes.c_double, p, p]
         lib.zero_step_units_clip_noalloc.restype = ctypes.c_int
+        lib.zero_step_units_host.argtypes = [ctypes.POINTER(ZeroUnit), i32, p, p, i32, i32, hp,
+                                             i32, p, p, p]
+        lib.zero_step_units_host.restype = ctypes.c_int
         lib.zero1_accumulate.argtypes = [p, p, i32, lay, p]
         lib.zero1_accumulate.restype = ctypes.c_int
         lib.zero1_step.argtypes = [p, i32, p, p, p, p, i32, lay, hp, p]
@@ -323,6 +326,36 @@ def zero_step_units(units, micro_step: int, n_micro: int, hp, stream=None):
     _check(load().zero_step_units(arr, n, int(micro_step), int(n_micro),
                                   ctypes.byref(h) if h is not None else None, _stream(stream)),
            "zero_step_units")
+
+
+ZERO_HOST_GRADS_FREE = 1
+
+
+class HostTables:
+    """Host pointer tables of zero_step_units_host, marshalled once:
+    host_grads[u][k] (pinned host tensors or addresses) and host_params[u]
+    (pinned host tensors, addresses or None; the whole list may be None)."""
+
+    def __init__(self, host_grads, host_params=None):
+        self._rows = [_ptrs(g) for g in host_grads]
+        self.grads = (ctypes.c_void_p * max(len(self._rows), 1))(
+            *[ctypes.cast(r, ctypes.c_void_p) for r in self._rows])
+        self.params = _ptrs(host_params) if host_params is not None else None
+
+
+def zero_step_units_host(units, host, micro_step: int, n_micro: int, hp, flags: int = 0,
+                         h2d_stream=None, compute_stream=None, d2h_stream=None):
+    """zero_step_units with the gradients copied in from pinned host memory
+    and the gathered parameters copied back out.  host: a HostTables, or a
+    (host_grads, host_params) pair."""
+    arr, keep, n = _units_arg(units)
+    if not isinstance(host, HostTables):
+        host = HostTables(*host)
+    h = _hp(hp)
+    _check(load().zero_step_units_host(arr, n, host.grads, host.params, int(micro_step),
+                                       int(n_micro), ctypes.byref(h) if h is not None else None,
+                                       int(flags), _stream(h2d_stream), _stream(compute_stream),
+                                       _stream(d2h_stream)), "zero_step_units_host")
 
 
 def zero_clip_workspace_bytes(units, n_micro: int = 1) -> int:

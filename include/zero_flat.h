@@ -319,6 +319,43 @@ int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t
                               int64_t* bytes);
 
 /*
+ * zero_step_units_host -- device, with host buffers.  zero_step_units for a
+ * caller whose gradients arrive in host memory and who wants the gathered
+ * parameters back in host memory: the end-to-end form of the step.  On one
+ * GPU the host link carries what the pages' interconnect carries, the
+ * reduce-scatter's input and the all-gather's output ([L5] section 3: one
+ * reduce-scatter in, one all-gather out per step).
+ *   host_grads[u][k]  pinned host memory: rank k's gradient of unit u, as
+ *                     many bf16 elements as units[u].grads[k] holds
+ *                     (numel_padded, or numel for an unpadded layout); copied
+ *                     into units[u].grads[k] on h2d_stream
+ *   host_params       NULL, or [n_units] pinned host buffers (NULL entries
+ *                     allowed): when the optimizer runs (micro_step ==
+ *                     n_micro), units[u].full_params[0] is copied into
+ *                     host_params[u] on d2h_stream once the step is done
+ *   flags             0, or ZERO_HOST_GRADS_FREE: by default the copies first
+ *                     wait for the work already queued on compute_stream,
+ *                     which may still read the device gradient buffers; with
+ *                     the flag the caller guarantees those buffers are free
+ *                     (for instance it alternates two sets of gradient buffers
+ *                     and orders h2d_stream itself), so that the next step's
+ *                     copies overlap this step's update
+ * The step itself runs on compute_stream once every copy has landed.  A unit
+ * whose rank rows are evenly spaced in both memories moves with one 2D copy,
+ * otherwise with one copy per rank.  The call returns when everything is
+ * queued; synchronize d2h_stream (compute_stream if host_params is NULL)
+ * before reading the results.  The library allocates no memory; it creates and
+ * releases the events that order the three streams.
+ * Errors: as zero_step_units; ZERO_ERR_INVALID_ARG for a NULL host_grads row;
+ * ZERO_ERR_CUDA if a copy cannot be queued.
+ */
+#define ZERO_HOST_GRADS_FREE 1
+int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
+                         const uint16_t* const* const* host_grads, uint16_t* const* host_params,
+                         int32_t micro_step, int32_t n_micro, const zero_adamw_t* hp,
+                         int32_t flags, void* h2d_stream, void* compute_stream, void* d2h_stream);
+
+/*
  * zero_step_units_clip_noalloc -- device.  The same computation as
  * zero_step_units_clip for callers that cannot allocate device memory for the
  * workspace: a runtime that gives all device memory to its own pool at

@@ -149,3 +149,25 @@ def test_error_message_is_per_call(lib):
     assert "n_tensors" in zf.zero_last_error()
     zf.zero_flat_layout([3], 1)
     assert zf.zero_last_error() == ""
+
+
+def test_host_step_rejects_bad_arguments_before_any_copy(lib):
+    """zero_step_units_host validates everything before it queues a copy: a
+    NULL host gradient row, unknown flags and a broken layout are rejected
+    (the fake addresses are never dereferenced)."""
+    off, L = zf.zero_flat_layout([100], 4)
+    good = [0x10000 * (i + 1) for i in range(4)]
+    unit = (good, good, good, good, None, [0x90000], L)
+    host_ok = [[0x200000 * (i + 1) for i in range(4)]]
+    host_null = [[0x200000, 0, 0x600000, 0x800000]]
+    with pytest.raises(zf.ZeroError) as ei:
+        zf.zero_step_units_host([unit], (host_null, None), 1, 1, HP, 0, 0, 0, 0)
+    assert ei.value.code == -1 and "NULL gradient" in zf.zero_last_error()
+    with pytest.raises(zf.ZeroError) as ei:
+        zf.zero_step_units_host([unit], (host_ok, None), 1, 1, HP, 6, 0, 0, 0)
+    assert ei.value.code == -1 and "flags" in zf.zero_last_error()
+    broken = zf.ZeroLayout(L.n_tensors, L.numel, L.numel_padded + 4, L.shard_numel + 1, 4, 0)
+    with pytest.raises(zf.ZeroError) as ei:
+        zf.zero_step_units_host([(good, good, good, good, None, [0x90000], broken)],
+                                (host_ok, None), 1, 1, HP, 0, 0, 0, 0)
+    assert ei.value.code == -3
