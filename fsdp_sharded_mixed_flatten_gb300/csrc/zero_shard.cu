@@ -172,7 +172,25 @@ cudaError_t launch_flatten(const FlatArgs& a, int elem_bytes, int unflatten, cud
 
 // ZeRO-1 local accumulation: rank k's full fp32 accumulator (P_pad elements)
 // plus its own bf16 gradient, element by element (no exchange between ranks).
-// blockIdx.y is the rank; 8 elements per thread, 16-byte loads and stores.
+// blockIdx.y is the rank; 8 elements per group, 16-byte loads and stores.
+// Each thread issues the loads of kZ1Unroll groups before it adds and stores
+// any of them, so that enough bytes are in flight to cover HBM latency.
+constexpr int kZ1Unroll = 4;
+
+template <int FIRST>
+__device__ __forceinline__ void z1_group(const uint4 w, const float (&o)[8], float* dst) {
+    float x[8];
+    const float2 p0 = bf16x2_to_float2(w.x), p1 = bf16x2_to_float2(w.y);
+    const float2 p2 = bf16x2_to_float2(w.z), p3 = bf16x2_to_float2(w.w);
+    x[0] = p0.x; x[1] = p0.y; x[2] = p1.x; x[3] = p1.y;
+    x[4] = p2.x; x[5] = p2.y; x[6] = p3.x; x[7] = p3.y;
+    if constexpr (!FIRST) {
+#pragma unroll
+        for (int t = 0; t < kVec; ++t) x[t] = __fadd_rn(o[t], x[t]);
+    }
+    st_f32x8(dst, x);
+}
+
 template <int MAXR, int FIRST>
 __global__ void __launch_bounds__(kThreads)
 zero1_accumulate_kernel(const __grid_constant__ StepArgs<MAXR> a) {
@@ -181,21 +199,24 @@ zero1_accumulate_kernel(const __grid_constant__ StepArgs<MAXR> a) {
     float* acc = a.accum[k];
     const int64_t groups = a.P_pad / kVec;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
-    for (int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; q < groups;
-         q += stride) {
-        const uint4 w = ld_stream(g + q * kVec);
-        float x[8];
-        const float2 p0 = bf16x2_to_float2(w.x), p1 = bf16x2_to_float2(w.y);
-        const float2 p2 = bf16x2_to_float2(w.z), p3 = bf16x2_to_float2(w.w);
-        x[0] = p0.x; x[1] = p0.y; x[2] = p1.x; x[3] = p1.y;
-        x[4] = p2.x; x[5] = p2.y; x[6] = p3.x; x[7] = p3.y;
-        if constexpr (!FIRST) {
-            float o[8];
-            ld_f32x8(acc + q * kVec, o);
+    int64_t q = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; q + (kZ1Unroll - 1) * stride < groups; q += kZ1Unroll * stride) {
+        uint4 w[kZ1Unroll];
+        float o[kZ1Unroll][8];
 #pragma unroll
-            for (int t = 0; t < kVec; ++t) x[t] = __fadd_rn(o[t], x[t]);
+        for (int u = 0; u < kZ1Unroll; ++u) w[u] = ld_stream(g + (q + u * stride) * kVec);
+        if constexpr (!FIRST) {
+#pragma unroll
+            for (int u = 0; u < kZ1Unroll; ++u) ld_f32x8(acc + (q + u * stride) * kVec, o[u]);
         }
-        st_f32x8(acc + q * kVec, x);
+#pragma unroll
+        for (int u = 0; u < kZ1Unroll; ++u) z1_group<FIRST>(w[u], o[u], acc + (q + u * stride) * kVec);
+    }
+    for (; q < groups; q += stride) {
+        const uint4 w = ld_stream(g + q * kVec);
+        float o[8];
+        if constexpr (!FIRST) ld_f32x8(acc + q * kVec, o);
+        z1_group<FIRST>(w, o, acc + q * kVec);
     }
     const int64_t tail0 = groups * kVec;
     if (blockIdx.x == 0 && tail0 + threadIdx.x < a.P_pad) {
