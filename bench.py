@@ -368,21 +368,25 @@ def time_e2e(res, steps, warmup, ws, device):
     return el, h2d, d2h
 
 
+def _oracle_sample(E, workload="gpt2-small"):
+    """Seeded inputs of one contiguous sample of E flat elements x N_d ranks
+    of a workload, for the CPU oracle."""
+    import numpy as np
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    w = synthetic.workload(workload)
+    g = synthetic.make_grads(E, w.n_ranks, w.grad_std, ("cpu-sample",))
+    master = synthetic.make_master_flat(E, w.n_ranks, w.master_std, ("cpu-sample",)).numpy()
+    return w, synthetic.bf16_bits(g), master, np.zeros_like(master), np.zeros_like(master)
+
+
 def cpu_baseline(seconds=8.0):
     """The CPU oracle as it stands, on a bounded contiguous sample of the
     gpt2-small workload (first unit, all 8 ranks), single-threaded."""
-    import numpy as np
-    import torch
     from fsdp_sharded_mixed_flatten_gb300 import synthetic
     from oracle import Oracle
     o = Oracle()
-    w = synthetic.workload("gpt2-small")
     E = 1 << 20
-    g = synthetic.make_grads(E, w.n_ranks, w.grad_std, ("cpu-sample",))
-    gb = synthetic.bf16_bits(g)
-    master = synthetic.make_master_flat(E, w.n_ranks, w.master_std, ("cpu-sample",)).numpy()
-    m = np.zeros_like(master)
-    v = np.zeros_like(master)
+    w, gb, master, m, v = _oracle_sample(E)
     hp = synthetic.ADAMW_DEFAULTS
     reps, t0, step = 0, time.perf_counter(), 0
     while True:
@@ -400,18 +404,46 @@ def cpu_baseline(seconds=8.0):
 
 # ----------------------------------------------------------------- arms ----
 
-def run_reference(args, ws, rank):
+def run_reference(args, ws, rank, budget_s=90.0):
+    """The oracle as the reference arm: W untimed and K timed steps, each over
+    a contiguous sample of the workload sized (from a short calibration) so
+    that the whole run stays within about budget_s seconds."""
     if rank != 0:
         return 0
-    base = cpu_baseline(seconds=max(2.0, 1.5 * args.steps))
-    line = {"metric": METRIC, "value": base["value"], "unit": UNIT, "n_gpus": args.gpus,
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    from oracle import Oracle
+    o = Oracle()
+    hp = synthetic.ADAMW_DEFAULTS
+    w, gb, master, m, v = _oracle_sample(1 << 16, args.workload)
+    t0 = time.perf_counter()
+    o.sampled_step(gb, master, m, v, step=1, **hp)
+    o.sampled_step(gb, master, m, v, step=2, **hp)
+    rate = 2 * (1 << 16) / (time.perf_counter() - t0)       # elements per second
+    E = int(budget_s * rate / (args.steps + args.warmup))
+    E = max(1 << 10, min(1 << 20, E)) & ~7
+    w, gb, master, m, v = _oracle_sample(E, args.workload)
+    step = 0
+    for _ in range(args.warmup):
+        step += 1
+        o.sampled_step(gb, master, m, v, step=step, **hp)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step += 1
+        o.sampled_step(gb, master, m, v, step=step, **hp)
+    el = time.perf_counter() - t0
+    value = E * args.steps / el
+    sample = (f"{E} contiguous flat elements x {w.n_ranks} ranks of the {args.workload} workload "
+              f"per step, {args.steps} timed oracle steps in {el:.1f} s (single thread, double "
+              f"arithmetic)")
+    line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
-            "ms_per_step": None, "higher_is_better": True, "scaling": "weak",
+            "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": workload_label(args.workload), "sample": base["sample"]},
-            "cpu_baseline": base,
-            "e2e": {"value": base["value"], "unit": UNIT, "h2d_bytes_per_step": 0,
+            "config": {"workload": workload_label(args.workload), "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
     return 0
