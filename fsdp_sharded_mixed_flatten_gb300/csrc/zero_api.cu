@@ -971,14 +971,19 @@ ZERO_API int zero1_accumulate(const uint16_t* const* grads, float* const* full_a
         }
         return ZERO_OK;
     };
+    const bool staged = use_staged();
     if (n <= 64) {
         static thread_local zf::StepArgs<64> a;
         go(a);
-        return cuda_status(zf::launch_zero1_accumulate<64>(a, first, st), "accumulate launch");
+        return cuda_status(staged ? zf::launch_zero1_accumulate_staged<64>(a, first, st)
+                                  : zf::launch_zero1_accumulate<64>(a, first, st),
+                           "accumulate launch");
     }
     static thread_local zf::StepArgs<512> a;
     go(a);
-    return cuda_status(zf::launch_zero1_accumulate<512>(a, first, st), "accumulate launch");
+    return cuda_status(staged ? zf::launch_zero1_accumulate_staged<512>(a, first, st)
+                              : zf::launch_zero1_accumulate<512>(a, first, st),
+                       "accumulate launch");
 }
 
 ZERO_API int zero1_step(const float* const* full_accum, int32_t n_micro, float* const* master,

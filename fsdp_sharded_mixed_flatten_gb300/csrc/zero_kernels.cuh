@@ -155,6 +155,10 @@ cudaError_t launch_staged_step_f32(const MultiArgs& a, int n_ptrs, cudaStream_t 
 // accumulator (a.grads -> a.accum, P_pad elements each).
 template <int MAXR>
 cudaError_t launch_zero1_accumulate(const StepArgs<MAXR>& a, int first, cudaStream_t stream);
+// The same through the bulk-copy pipeline (the default; the register kernel
+// above runs under ZERO_STEP_KERNEL=direct).
+template <int MAXR>
+cudaError_t launch_zero1_accumulate_staged(const StepArgs<MAXR>& a, int first, cudaStream_t stream);
 // Grid a staged launch of `mode` over `total_tiles` tiles uses (persistent:
 // at most one CTA per SM); norm launches write this many partial sums.
 int staged_grid(int mode, int total_tiles);

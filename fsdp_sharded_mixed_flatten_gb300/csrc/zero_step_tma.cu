@@ -799,6 +799,157 @@ cudaError_t launch_staged_step(const MultiArgs& a, int n_ptrs, int mode, cudaStr
     }
 }
 
+// ---------------------------------------------------------------------------
+// ZeRO-1 local accumulation through the same bulk-copy pipeline: rank k's full
+// fp32 accumulator += rank k's bf16 gradient, element by element (no exchange
+// between ranks).  A tile is 4096 elements of one rank's buffers; the producer
+// lane copies the tile's gradient (8 KB) and, after the first micro-step, its
+// accumulator (16 KB) into a ring of eight 24 KB stages, so that up to 192 KB
+// per SM are in flight whatever the consumers' registers hold.  Consumers add
+// in fp32 (exact adds, the same as the register kernel) and store the
+// accumulator with 16-byte streaming stores.
+constexpr int kZ1Stages = 8;
+constexpr int kZ1GradBytes = kStagedTile * 2;                  // 8192
+constexpr int kZ1StageBytes = kZ1GradBytes + kStagedTile * 4;  // 24576
+constexpr size_t kZ1Smem = static_cast<size_t>(kZ1Stages) * kZ1StageBytes;
+
+template <int MAXR, int FIRST>
+__global__ void __launch_bounds__(kTmaThreads, 1)
+zero1_accumulate_staged_kernel(const __grid_constant__ StepArgs<MAXR> a) {
+    extern __shared__ __align__(128) uint8_t smem[];
+    __shared__ __align__(8) uint64_t full[kZ1Stages];
+    __shared__ __align__(8) uint64_t empty[kZ1Stages];
+    __shared__ int abort_flag;
+    __shared__ uint32_t issued;
+    __shared__ unsigned int consumed_min;
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kZ1Stages; ++i) {
+            mbar_init(smem_u32(&full[i]), 1);
+            mbar_init(smem_u32(&empty[i]), kConsumerWarps);
+        }
+        abort_flag = 0;
+        issued = 0;
+        consumed_min = 0xFFFFFFFFu;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncthreads();
+    const int64_t tpr = (a.P_pad + kStagedTile - 1) / kStagedTile;
+    const int64_t total = tpr * a.n_ranks;
+    if (threadIdx.x >= kConsumers) {
+        if (threadIdx.x == kConsumers) {
+            uint32_t it = 0;
+            for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+                const int k = static_cast<int>(tile / tpr);
+                const int64_t e0 = (tile - k * tpr) * kStagedTile;
+                const int64_t n = a.P_pad - e0 < kStagedTile ? a.P_pad - e0 : kStagedTile;
+                const uint32_t gbytes = static_cast<uint32_t>(n & ~7LL) * 2;
+                const uint32_t abytes = FIRST ? 0u : static_cast<uint32_t>(n & ~3LL) * 4;
+                const uint32_t slot = it % kZ1Stages, parity = ((it / kZ1Stages) & 1) ^ 1;
+                if (!mbar_wait_bounded(smem_u32(&empty[slot]), parity, &abort_flag, kWaitLimitNs))
+                    break;
+                const uint32_t bar = smem_u32(&full[slot]);
+                const uint32_t dst = smem_u32(smem + slot * kZ1StageBytes);
+                mbar_arrive_expect_tx(bar, gbytes + abytes);
+                if (gbytes > 0) bulk_copy_g2s(dst, a.grads[k] + e0, gbytes, bar);
+                if (abytes > 0) bulk_copy_g2s(dst + kZ1GradBytes, a.accum[k] + e0, abytes, bar);
+                ++it;
+            }
+            issued = it;
+        }
+    } else {
+        const int tid = threadIdx.x;
+        const int lane = tid & 31;
+        const int first = tid * kVec;
+        uint32_t it = 0;
+        for (int64_t tile = blockIdx.x; tile < total; tile += gridDim.x) {
+            const int k = static_cast<int>(tile / tpr);
+            const int64_t e0 = (tile - k * tpr) * kStagedTile;
+            const int64_t n = a.P_pad - e0 < kStagedTile ? a.P_pad - e0 : kStagedTile;
+            const int nv = static_cast<int>(n - first < kVec ? (n - first > 0 ? n - first : 0) : kVec);
+            const uint32_t slot = it % kZ1Stages, parity = (it / kZ1Stages) & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[slot]), parity,
+                                                           &abort_flag, kWaitLimitNs)))
+                break;
+            const uint8_t* stage = smem + slot * kZ1StageBytes;
+            float* acc = a.accum[k] + e0 + first;
+            float x[8];
+            if (nv == kVec) {
+                // a whole group lies inside both copied ranges
+                const uint4 w = *reinterpret_cast<const uint4*>(stage + first * 2);
+                const float2 p0 = bf16x2_to_float2(w.x), p1 = bf16x2_to_float2(w.y);
+                const float2 p2 = bf16x2_to_float2(w.z), p3 = bf16x2_to_float2(w.w);
+                x[0] = p0.x; x[1] = p0.y; x[2] = p1.x; x[3] = p1.y;
+                x[4] = p2.x; x[5] = p2.y; x[6] = p3.x; x[7] = p3.y;
+                if constexpr (!FIRST) {
+                    // threads 4-7 of every 8 read their upper 16 bytes first, so
+                    // that each quarter-warp's reads fall in distinct banks
+                    const float4* p =
+                        reinterpret_cast<const float4*>(stage + kZ1GradBytes + first * 4);
+                    const int sw = (tid >> 2) & 1;
+                    const float4 ya = p[sw], yb = p[sw ^ 1];
+                    const float4 o0 = sw ? yb : ya, o1 = sw ? ya : yb;
+                    x[0] = __fadd_rn(o0.x, x[0]); x[1] = __fadd_rn(o0.y, x[1]);
+                    x[2] = __fadd_rn(o0.z, x[2]); x[3] = __fadd_rn(o0.w, x[3]);
+                    x[4] = __fadd_rn(o1.x, x[4]); x[5] = __fadd_rn(o1.y, x[5]);
+                    x[6] = __fadd_rn(o1.z, x[6]); x[7] = __fadd_rn(o1.w, x[7]);
+                }
+            } else {
+                // the end of the buffer: plain reads of what the copies left out
+                const uint16_t* g = a.grads[k] + e0 + first;
+#pragma unroll
+                for (int t = 0; t < kVec; ++t) {
+                    x[t] = 0.0f;
+                    if (t < nv) x[t] = FIRST ? bf16_to_float(g[t]) : __fadd_rn(acc[t], bf16_to_float(g[t]));
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&empty[slot]));
+            ++it;
+            if (nv == kVec) {
+                st_f32x8(acc, x);
+            } else {
+#pragma unroll
+                for (int t = 0; t < kVec; ++t) {
+                    if (t < nv) acc[t] = x[t];
+                }
+            }
+        }
+        if (lane == 0) atomicMin(&consumed_min, it);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0 && abort_flag) {
+        // Let every copy this CTA issued land before shared memory goes away.
+        for (uint32_t it = consumed_min; it < issued; ++it) {
+            const uint32_t slot = it % kZ1Stages, parity = (it / kZ1Stages) & 1;
+            int dummy = 0;
+            mbar_wait_bounded(smem_u32(&full[slot]), parity, &dummy, kDrainLimitNs);
+        }
+    }
+}
+
+template <int MAXR>
+cudaError_t launch_zero1_accumulate_staged(const StepArgs<MAXR>& a, int first,
+                                           cudaStream_t stream) {
+    const int64_t tiles = (a.P_pad + kStagedTile - 1) / kStagedTile * a.n_ranks;
+    if (tiles <= 0) return cudaSuccess;
+    const void* kfn = first ? reinterpret_cast<const void*>(&zero1_accumulate_staged_kernel<MAXR, 1>)
+                            : reinterpret_cast<const void*>(&zero1_accumulate_staged_kernel<MAXR, 0>);
+    cudaError_t e = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(kZ1Smem));
+    if (e != cudaSuccess) return e;
+    const int grid = persistent_grid(kfn, kTmaThreads, kZ1Smem, tiles);
+    if (first) {
+        zero1_accumulate_staged_kernel<MAXR, 1><<<grid, kTmaThreads, kZ1Smem, stream>>>(a);
+    } else {
+        zero1_accumulate_staged_kernel<MAXR, 0><<<grid, kTmaThreads, kZ1Smem, stream>>>(a);
+    }
+    return cudaGetLastError();
+}
+
+template cudaError_t launch_zero1_accumulate_staged<64>(const StepArgs<64>&, int, cudaStream_t);
+template cudaError_t launch_zero1_accumulate_staged<512>(const StepArgs<512>&, int, cudaStream_t);
+
 // A barrier that nothing completes: the bounded wait must run out, record the
 // timeout and let the kernel return.
 __global__ void wait_timeout_selftest_kernel(uint64_t limit_ns) {
