@@ -274,6 +274,100 @@ class Resident:
         return self.launches_per_step
 
 
+class PerParamResident:
+    """The workload as FSDP2 per-parameter units: every tensor its own unit,
+    split along dim 0 into N_d chunks with no padding (Shard(0)), all stepped
+    by one zero_step_units call (the library packs them into launches)."""
+
+    def __init__(self, w):
+        import torch
+        from fsdp_sharded_mixed_flatten_gb300 import synthetic
+        from fsdp_sharded_mixed_flatten_gb300.buffers import ParamUnit
+        from fsdp_sharded_mixed_flatten_gb300.zero import prepare_units
+        self.w = w
+        self.n_micro = 1
+        self.units = []
+        for u in w.units:
+            for i, (d0, row) in enumerate(u.rows()):
+                pu = ParamUnit(d0, row, w.n_ranks)
+                pu.set_master_flat(synthetic.make_master_flat(
+                    pu.numel, 1, w.master_std, (w.name, u.name, "param", i), device="cuda"))
+                for r in range(w.n_ranks):
+                    synthetic.fill_grad_(pu.grads[r], pu.numel, w.grad_std,
+                                         synthetic.seed_for(w.name, u.name, "param", i, "grad", r),
+                                         w.outlier_frac, w.outlier_scale)
+                self.units.append(pu)
+        torch.cuda.synchronize()
+        self.numel = sum(pu.numel for pu in self.units)
+        # every element once: N_d bf16 gradients, fp32 state read + written, bf16 output
+        self.bytes = sum(pu.numel * (2 * w.n_ranks + 26) for pu in self.units)
+        self.prepared = prepare_units([pu.unit_tuple() for pu in self.units])
+        self.launches_per_step = staged_launches([w.n_ranks] * len(self.units))
+
+    def launch(self, step, hp_base, events=None):
+        from fsdp_sharded_mixed_flatten_gb300 import zero_step_units
+        if events is not None:
+            events[0][0].record()
+        zero_step_units(self.prepared, 1, 1, dict(hp_base, step=step))
+        if events is not None:
+            events[0][1].record()
+        return self.launches_per_step
+
+
+class ClipResident(Resident):
+    """Resident units stepped with global gradient-norm clipping: a norm pass
+    (the averaged gradient written to each unit's accumulator with per-CTA
+    partial sums of squares) and an update pass (AdamW from the accumulator
+    times the clip coefficient)."""
+
+    def __init__(self, w, max_norm):
+        import torch
+        from fsdp_sharded_mixed_flatten_gb300 import zero_clip_workspace_bytes
+        from fsdp_sharded_mixed_flatten_gb300.buffers import aligned_rows
+        from fsdp_sharded_mixed_flatten_gb300.zero import prepare_units
+        super().__init__(w)
+        for fu in self.units:
+            fu.accum = aligned_rows(fu.n_ranks, fu.S, torch.float32, "cuda", 0)
+        self.prepared = prepare_units([(fu.grad_rows(), *fu.state_rows(), fu.accum_rows(),
+                                        fu.param_rows(), fu.layout) for fu in self.units])
+        self.ws_bytes = zero_clip_workspace_bytes(self.prepared, 1)
+        self.workspace = torch.empty(max(self.ws_bytes // 8, 1), dtype=torch.float64,
+                                     device="cuda")
+        self.norm = torch.zeros(1, dtype=torch.float32, device="cuda")
+        self.max_norm = max_norm
+        # pass 1: gradients in, averaged gradient out; pass 2: it and the state in, state
+        # and parameters out
+        self.bytes = sum(fu.P_pad * ((2 * fu.n_ranks + 4) + (4 + 24 + 2)) for fu in self.units)
+        nr = [fu.n_ranks for fu in self.units]
+        self.launches_per_step = (staged_launches(nr, pointers=lambda n: 2 * n)
+                                  + staged_launches(nr, pointers=lambda n: 4 * n + 1))
+
+    def launch(self, step, hp_base, events=None):
+        from fsdp_sharded_mixed_flatten_gb300 import zero_step_units_clip
+        if events is not None:
+            events[0][0].record()
+        zero_step_units_clip(self.prepared, 1, 1, dict(hp_base, step=step), self.max_norm,
+                             self.workspace, self.ws_bytes, self.norm)
+        if events is not None:
+            events[0][1].record()
+        return self.launches_per_step
+
+
+def timed_extra(res, steps, warmup, ws, device, hbm_peak):
+    import gc
+    import torch
+    el, kern, launches, _ = time_resident(res, steps, warmup, ws, device)
+    gbs = res.bytes * steps / kern / 1e9
+    out = {"params_per_s": ws * res.numel * steps / el, "ms_per_step": el / steps * 1e3,
+           "kernel_gbs": gbs, "frac_of_measured_hbm": gbs / hbm_peak,
+           "bytes_per_step": res.bytes, "units": len(res.units), "n_ranks": res.w.n_ranks,
+           "params": res.numel, "launches_per_step": res.launches_per_step, "steps": steps}
+    del res
+    gc.collect()
+    torch.cuda.empty_cache()
+    return out
+
+
 def time_resident(res, steps, warmup, ws, device, per_kernel=True, clocks=None):
     import torch
     from fsdp_sharded_mixed_flatten_gb300 import synthetic
@@ -622,6 +716,13 @@ def run_ours(args, ws, rank, local):
                                                                   hbm_peak, shared=True)
 
         extra["llama3-8b-layer-K4-zero2-vs-zero1"] = zero1_vs_zero2(device, hbm_peak)
+        from fsdp_sharded_mixed_flatten_gb300 import synthetic as _syn
+        extra["gpt2-small-global-norm-clip"] = timed_extra(
+            ClipResident(_syn.workload("gpt2-small"), max_norm=1.0), 20, 3, ws, device, hbm_peak)
+        extra["gpt2-small-fsdp2-per-parameter-148-units"] = timed_extra(
+            PerParamResident(_syn.workload("gpt2-small")), 20, 3, ws, device, hbm_peak)
+        extra["llama3-8b-layer-fsdp2-per-parameter-9-units"] = timed_extra(
+            PerParamResident(_syn.workload("llama3-8b-layer")), 5, 3, ws, device, hbm_peak)
 
     base = cpu_baseline() if (rank == 0 and ws == 1 and not args.no_cpu) else None
     line = {

@@ -18,7 +18,7 @@ from typing import List, Sequence
 
 import torch
 
-from .zero import ZeroLayout, zero_flat_layout
+from .zero import ZeroLayout, zero_flat_layout, zero_param_layout, zero_shard_numel
 
 ROW_ALIGN = 128   # elements: 256 B for bf16, 512 B for fp32
 
@@ -86,3 +86,34 @@ class FlatUnit:
     def state_bytes(self) -> int:
         n = 3 + (1 if self.accum is not None else 0)
         return n * self.n_ranks * self.S * 4
+
+
+class ParamUnit:
+    """Buffers of one parameter under the per-parameter Shard(0) layout
+    (FSDP2): no FlatParameter and no padding.  Rank k's gradient and the
+    gathered parameter hold exactly numel elements; rank r's state holds its
+    chunk of ceil(dim0 / N_d) rows (fewer, or none, at the end)."""
+
+    def __init__(self, dim0: int, row: int, n_ranks: int, device="cuda"):
+        self.layout = zero_param_layout(dim0, row, n_ranks)
+        self.n_ranks = int(n_ranks)
+        self.numel = int(dim0) * int(row)
+        self.sizes = [zero_shard_numel(self.layout, r) for r in range(n_ranks)]
+        self.grads = aligned_rows(n_ranks, self.numel, torch.bfloat16, device, 0)
+        width = max(max(self.sizes), 1)
+        self.master = aligned_rows(n_ranks, width, torch.float32, device, 0)
+        self.m = aligned_rows(n_ranks, width, torch.float32, device, 0)
+        self.v = aligned_rows(n_ranks, width, torch.float32, device, 0)
+        self.accum = None
+        self.params = aligned_rows(1, self.numel, torch.bfloat16, device, 0)
+
+    def set_master_flat(self, flat: torch.Tensor):
+        """Scatter a (numel,) fp32 vector into the rank shards."""
+        off = 0
+        for r, n in enumerate(self.sizes):
+            self.master[r, :n].copy_(flat[off:off + n])
+            off += n
+
+    def unit_tuple(self):
+        return (rows(self.grads), rows(self.master), rows(self.m), rows(self.v), None,
+                rows(self.params), self.layout)

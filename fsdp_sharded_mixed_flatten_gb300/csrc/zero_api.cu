@@ -720,15 +720,23 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
         const int64_t width = count * static_cast<int64_t>(sizeof(uint16_t));
         int64_t dpitch = 0, spitch = 0;
         cudaError_t e = cudaSuccess;
-        if (evenly_spaced(x.grads, n, width, &dpitch) &&
+        bool done = false;
+        if (n > 1 && evenly_spaced(x.grads, n, width, &dpitch) &&
             evenly_spaced(host_grads[i], n, width, &spitch)) {
-            e = n == 1 ? cudaMemcpyAsync(const_cast<uint16_t*>(x.grads[0]), host_grads[i][0],
-                                         static_cast<size_t>(width), cudaMemcpyHostToDevice, h2d)
-                       : cudaMemcpy2DAsync(const_cast<uint16_t*>(x.grads[0]),
-                                           static_cast<size_t>(dpitch), host_grads[i][0],
-                                           static_cast<size_t>(spitch), static_cast<size_t>(width),
-                                           static_cast<size_t>(n), cudaMemcpyHostToDevice, h2d);
-        } else {
+            // Evenly spaced rows need not lie in one allocation (separate
+            // buffers can land at a regular stride): the runtime then rejects
+            // the 2D copy before queuing anything, and the rows go one by one.
+            e = cudaMemcpy2DAsync(const_cast<uint16_t*>(x.grads[0]), static_cast<size_t>(dpitch),
+                                  host_grads[i][0], static_cast<size_t>(spitch),
+                                  static_cast<size_t>(width), static_cast<size_t>(n),
+                                  cudaMemcpyHostToDevice, h2d);
+            done = e == cudaSuccess;
+            if (e == cudaErrorInvalidValue) {
+                (void)cudaGetLastError();
+                e = cudaSuccess;
+            }
+        }
+        if (!done) {
             for (int k = 0; k < n && e == cudaSuccess; ++k) {
                 e = cudaMemcpyAsync(const_cast<uint16_t*>(x.grads[k]), host_grads[i][k],
                                     static_cast<size_t>(width), cudaMemcpyHostToDevice, h2d);

@@ -41,13 +41,22 @@ ADAMW_DEFAULTS = dict(lr=1e-3, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.
 
 @dataclasses.dataclass(frozen=True)
 class Unit:
-    """One FSDP unit: its tensors' element counts in registration order."""
+    """One FSDP unit: its tensors' element counts in registration order, and
+    optionally their shapes as (dim 0, elements per dim-0 row) -- what a
+    per-parameter Shard(0) layout splits."""
     name: str
     numels: tuple
+    shapes: tuple = ()
 
     @property
     def numel(self) -> int:
         return int(sum(self.numels))
+
+    def rows(self):
+        """(dim0, row_numel) of every tensor; a 1-D tensor is dim0 rows of 1."""
+        if self.shapes:
+            return list(self.shapes)
+        return [(int(n), 1) for n in self.numels]
 
 
 @dataclasses.dataclass(frozen=True)
@@ -67,29 +76,36 @@ class Workload:
         return sum(u.numel for u in self.units)
 
 
+def _unit(name: str, shapes) -> Unit:
+    return Unit(name, tuple(a * b for a, b in shapes), tuple(shapes))
+
+
 def _gpt2_block(i: int, d: int = 768) -> Unit:
-    return Unit(f"h.{i}", (
-        d, d,                      # ln_1 weight, bias
-        d * 3 * d, 3 * d,          # attn.c_attn weight, bias
-        d * d, d,                  # attn.c_proj weight, bias
-        d, d,                      # ln_2 weight, bias
-        d * 4 * d, 4 * d,          # mlp.c_fc weight, bias
-        4 * d * d, d,              # mlp.c_proj weight, bias
+    # GPT-2's Conv1D weights are stored (in, out)
+    return _unit(f"h.{i}", (
+        (d, 1), (d, 1),                # ln_1 weight, bias
+        (d, 3 * d), (3 * d, 1),        # attn.c_attn weight, bias
+        (d, d), (d, 1),                # attn.c_proj weight, bias
+        (d, 1), (d, 1),                # ln_2 weight, bias
+        (d, 4 * d), (4 * d, 1),        # mlp.c_fc weight, bias
+        (4 * d, d), (d, 1),            # mlp.c_proj weight, bias
     ))
 
 
 def gpt2_small_units() -> List[Unit]:
     d = 768
-    root = Unit("root", (50257 * d, 1024 * d, d, d))   # wte (tied), wpe, ln_f w/b
+    # wte (tied with the output head), wpe, ln_f weight and bias
+    root = _unit("root", ((50257, d), (1024, d), (d, 1), (d, 1)))
     return [_gpt2_block(i, d) for i in range(12)] + [root]
 
 
 def llama3_8b_layer_unit() -> Unit:
     d, ffn, kv = 4096, 14336, 8 * 128
-    return Unit("layer", (
-        d * d, d * kv, d * kv, d * d,       # q, k, v, o projections
-        d * ffn, d * ffn, ffn * d,          # gate, up, down
-        d, d,                               # input and post-attention RMSNorm
+    # nn.Linear weights are stored (out, in)
+    return _unit("layer", (
+        (d, d), (kv, d), (kv, d), (d, d),       # q, k, v, o projections
+        (ffn, d), (ffn, d), (d, ffn),           # gate, up, down
+        (d, 1), (d, 1),                         # input and post-attention RMSNorm
     ))
 
 

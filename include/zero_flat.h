@@ -341,7 +341,8 @@ int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t
  *                     and orders h2d_stream itself), so that the next step's
  *                     copies overlap this step's update
  * The step itself runs on compute_stream once every copy has landed.  A unit
- * whose rank rows are evenly spaced in both memories moves with one 2D copy,
+ * whose rank rows are evenly spaced in both memories moves with one 2D copy
+ * when the runtime accepts one (rows of separate allocations may be rejected),
  * otherwise with one copy per rank.  The call returns when everything is
  * queued; synchronize d2h_stream (compute_stream if host_params is NULL)
  * before reading the results.  The library allocates no memory; it creates and
