@@ -337,8 +337,9 @@ int check_unit(const UnitView& u, int32_t micro_step, int32_t n_micro, bool opti
     return ZERO_OK;
 }
 
-int run_units(const UnitView* units, int n_units, int32_t micro_step, int32_t n_micro,
-              const zero_adamw_t* hp, cudaStream_t stream) {
+// Every check run_units makes before it launches anything.
+int validate_units(const UnitView* units, int n_units, int32_t micro_step, int32_t n_micro,
+                   const zero_adamw_t* hp) {
     // Every unit shares micro_step / n_micro; the optimizer runs unless this is
     // an accumulation-only micro-step.
     const bool micro = units[0].accum != nullptr && n_micro > 1;
@@ -351,6 +352,22 @@ int run_units(const UnitView* units, int n_units, int32_t micro_step, int32_t n_
             return fail(ZERO_ERR_INVALID_ARG, "either every unit has an accumulator or none");
         if (int rc = check_unit(units[i], micro_step, n_micro, optimizer_runs)) return rc;
     }
+    if (!use_staged()) {
+        for (int i = 0; i < n_units; ++i) {
+            if (unpadded(units[i].L))
+                return fail(ZERO_ERR_INVALID_ARG,
+                            "unpadded per-parameter layouts need the staged kernels "
+                            "(ZERO_STEP_KERNEL=direct is set)");
+        }
+    }
+    return ZERO_OK;
+}
+
+int run_units(const UnitView* units, int n_units, int32_t micro_step, int32_t n_micro,
+              const zero_adamw_t* hp, cudaStream_t stream) {
+    if (int rc = validate_units(units, n_units, micro_step, n_micro, hp)) return rc;
+    const bool micro = units[0].accum != nullptr && n_micro > 1;
+    const bool optimizer_runs = !(micro && micro_step < n_micro);
     if (use_staged()) {
         int mode = zf::kModePlain;
         if (micro) mode = micro_step < n_micro ? (micro_step > 1 ? zf::kModeRsAdd : zf::kModeRsStore)
@@ -358,12 +375,6 @@ int run_units(const UnitView* units, int n_units, int32_t micro_step, int32_t n_
         zf::AdamConsts k{};
         if (optimizer_runs) k = derive_consts(hp, micro ? static_cast<double>(n_micro) : 1.0);
         return launch_units_staged(units, n_units, mode, k, stream);
-    }
-    for (int i = 0; i < n_units; ++i) {
-        if (unpadded(units[i].L))
-            return fail(ZERO_ERR_INVALID_ARG,
-                        "unpadded per-parameter layouts need the staged kernels "
-                        "(ZERO_STEP_KERNEL=direct is set)");
     }
     for (int i = 0; i < n_units; ++i) {
         const UnitView& u = units[i];
@@ -706,6 +717,17 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
             if (host_grads[i][k] == nullptr || x.grads[k] == nullptr)
                 return fail(ZERO_ERR_INVALID_ARG, "unit %d rank %d: NULL gradient buffer", i, k);
         }
+    }
+    {
+        // every check of the step itself, before any copy is queued
+        static thread_local std::vector<UnitView> views;
+        views.resize(static_cast<size_t>(n_units));
+        for (int i = 0; i < n_units; ++i) {
+            const zero_unit_t& x = units[i];
+            views[i] = UnitView{x.layout, x.grads, x.master, x.m, x.v, x.accum, x.full_params,
+                                x.n_out};
+        }
+        if (int rc = validate_units(views.data(), n_units, micro_step, n_micro, hp)) return rc;
     }
     const auto h2d = static_cast<cudaStream_t>(h2d_stream);
     const auto comp = static_cast<cudaStream_t>(compute_stream);

@@ -23,9 +23,11 @@
  *
  * Conventions shared by every entry point
  *   - bf16 values travel as uint16_t bit patterns; fp32 as float.
- *   - Every buffer is owned by the caller.  The library allocates nothing
+ *   - Every buffer is owned by the caller.  The library allocates no memory
  *     and keeps no state between calls except one device status word (see
- *     zero_device_status); only zero_device_status synchronises a stream.
+ *     zero_device_status) and the 32 KB scratch array of
+ *     zero_step_units_clip_noalloc; only zero_device_status synchronises a
+ *     stream.
  *   - Device-side calls are asynchronous on `stream` (a cudaStream_t, or NULL
  *     for the legacy default stream) and return after the launch.  The return
  *     code covers argument checks and launch errors; completion and any later

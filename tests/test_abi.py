@@ -171,3 +171,12 @@ def test_host_step_rejects_bad_arguments_before_any_copy(lib):
         zf.zero_step_units_host([(good, good, good, good, None, [0x90000], broken)],
                                 (host_ok, None), 1, 1, HP, 0, 0, 0, 0)
     assert ei.value.code == -3
+    # the step's own checks also run before any copy is queued
+    with pytest.raises(zf.ZeroError) as ei:
+        zf.zero_step_units_host([unit], (host_ok, None), 1, 1, dict(HP, step=0), 0, 0, 0, 0)
+    assert ei.value.code == -1
+    bad = [0x10000 * (i + 1) + 2 for i in range(4)]
+    with pytest.raises(zf.ZeroError) as ei:
+        zf.zero_step_units_host([(good, bad, good, good, None, [0x90000], L)], (host_ok, None),
+                                1, 1, HP, 0, 0, 0, 0)
+    assert ei.value.code == -2
