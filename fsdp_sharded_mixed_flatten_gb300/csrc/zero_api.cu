@@ -1,8 +1,11 @@
 // Host side of the C ABI declared in include/zero_flat.h: argument checks,
-// FlatParameter layout, derivation of the fp32 kernel constants in double
-// precision, packing of the per-rank pointer tables into the launch arguments
-// and dispatch to the kernels.  The library allocates nothing and keeps no
-// state apart from a per-thread error message.
+// FlatParameter and per-parameter layouts, derivation of the fp32 kernel
+// constants in double precision, packing of the per-rank pointer tables into
+// the launch arguments, dispatch to the kernels, and the stream ordering of
+// the host-buffer step.  The library allocates no memory.  Its only state is
+// a per-thread error message, per-device caches of kernel attributes and
+// occupancy, and (device side) the status word and the scratch array of the
+// no-alloc clipped step.
 #include <cmath>
 #include <cstdarg>
 #include <cstdio>
