@@ -217,8 +217,19 @@ __device__ __forceinline__ TileGeom tile_geom(const A& a, int tile) {
     g.u = &a.unit[find_unit(a, tile)];
     const int local = tile - g.u->tile_begin;
     const int64_t S = g.u->S;
-    g.r = local / g.u->tiles_per_rank;
-    g.j0 = static_cast<int64_t>(local - g.r * g.u->tiles_per_rank) * kStagedTile;
+    // A unit's tiles: first every rank's full tiles (rank by rank), then the
+    // ranks' short last tiles.  A short tile costs a whole pass through the
+    // pipeline, so the short ones go to the end of the unit, where they fill
+    // the last round of the persistent CTAs instead of lengthening it.
+    const int full = static_cast<int>(S / kStagedTile);
+    const int n_full = full * g.u->n_ranks;
+    if (local < n_full) {
+        g.r = local / full;
+        g.j0 = static_cast<int64_t>(local - g.r * full) * kStagedTile;
+    } else {
+        g.r = local - n_full;
+        g.j0 = static_cast<int64_t>(full) * kStagedTile;
+    }
     g.e0 = static_cast<int64_t>(g.r) * S + g.j0;
     // valid elements: the tile, the rank's shard and the buffers all bound it
     // (an unpadded per-parameter layout ends before its last shards do)
