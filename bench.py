@@ -179,8 +179,8 @@ class ClockSampler:
 
 # Launch packing of zero_step_units (ZERO_UNITS_PER_LAUNCH, ZERO_POINTERS_PER_LAUNCH in
 # include/zero_flat.h): used only to report how many kernels a step launches.
-UNITS_PER_LAUNCH = 32
-POINTERS_PER_LAUNCH = 3712
+UNITS_PER_LAUNCH = 64
+POINTERS_PER_LAUNCH = 3392
 
 
 def staged_launches(n_ranks_per_unit, n_out=1, pointers=None):

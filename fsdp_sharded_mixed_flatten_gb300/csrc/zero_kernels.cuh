@@ -69,8 +69,8 @@ struct FlatArgs {
 // Bulk-copy staged kernels: argument block covering up to kMaxUnits units
 // (FlatParameters) whose per-rank pointers live in one flat table.
 constexpr int kStagedTile = 4096;   // shard elements per tile (512 consumers x 8)
-constexpr int kMaxUnits = 32;
-constexpr int kMaxPtrs = 3712;
+constexpr int kMaxUnits = 64;
+constexpr int kMaxPtrs = 3392;
 
 struct UnitDesc {
     int64_t S;

@@ -263,12 +263,12 @@ int zero_selftest_wait_timeout(int64_t limit_ns, void* stream);
  * with its own layout and buffers.  zero_step_units(units, n) computes exactly
  * what n calls of zero_step (one per unit, same micro_step / n_micro / hp)
  * compute, bit for bit, but packs the units into as few launches as the launch
- * argument block allows (up to 32 units and 3712 pointers per launch), so
+ * argument block allows (up to 64 units and 3392 pointers per launch), so
  * small units do not each pay a launch, a pipeline fill and a tail.
  * Either every unit has an accumulator or none does.
  */
-#define ZERO_UNITS_PER_LAUNCH 32      /* units packed into one launch at most          */
-#define ZERO_POINTERS_PER_LAUNCH 3712 /* device pointers per launch: per unit 4*N_d +    */
+#define ZERO_UNITS_PER_LAUNCH 64      /* units packed into one launch at most          */
+#define ZERO_POINTERS_PER_LAUNCH 3392 /* device pointers per launch: per unit 4*N_d +    */
                                       /* n_out (plain), 5*N_d + n_out (last micro-step), */
                                       /* 2*N_d (accumulation micro-step)                 */
 typedef struct zero_unit {

@@ -104,7 +104,7 @@ def test_clipped_step_accumulation(oracle):
 def test_clipped_many_units_several_norm_launches(oracle):
     """More units than one launch holds: the partial sums of several norm
     launches are reduced together."""
-    specs = [([3000 + 41 * i], 64) for i in range(16)] + [([2000 + i], 3) for i in range(30)]
+    specs = [([3000 + 41 * i], 64) for i in range(32)] + [([2000 + i], 3) for i in range(40)]
     run = ClipRun(specs, "clip-many")
     for t in (1, 2):
         run.step(oracle, t, 0.05)

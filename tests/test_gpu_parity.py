@@ -266,10 +266,10 @@ def _unit_tuple(u, accum):
     # GPT-2-small-like: 12 equal blocks + a bigger root unit (scaled down), N_d = 8
     [([768, 768, 9000, 300], 8)] * 12 + [([50000, 7000, 5], 8)],
     # more units than fit one launch, mixed rank counts and ragged shards
-    [([1000 + 37 * i], 1 + (i % 9)) for i in range(40)],
-    # pointer-limited packing: 64 ranks per unit -> at most 14 units per launch
+    [([1000 + 37 * i], 1 + (i % 9)) for i in range(80)],
+    # pointer-limited packing: 64 ranks per unit -> at most 13 units per launch
     [([64 * 53 + i], 64) for i in range(20)],
-], ids=["gpt2_like", "40_units_mixed", "pointer_limited"])
+], ids=["gpt2_like", "80_units_mixed", "pointer_limited"])
 def test_step_units_equals_per_unit_steps(kernel, specs, n_micro):
     """zero_step_units over many FlatParameters is bit-identical to one
     zero_step per unit."""
