@@ -579,8 +579,8 @@ def run_sweep(args, device, hbm_peak):
             w = synthetic.workload(f"sweep:{P}:{n}")
             res = Resident(w)
             fu = res.units[0]
-            steps = int(max(3, min(200, 2e10 // res.bytes)))
-            el, kern, _, _ = time_resident(res, steps, 3, 1, device)
+            steps = int(max(10, min(200, 2e10 // res.bytes)))
+            el, kern, _, _ = time_resident(res, steps, 5, 1, device)
             fused_gbs = res.bytes * steps / kern / 1e9
             gsh = aligned_rows(n, fu.S, torch.float32, device, 0)
             psh = aligned_rows(n, fu.S, torch.bfloat16, device, 0)
