@@ -58,10 +58,16 @@ def dist_env():
 
 
 def init_dist(ws, backend):
+    """Process group of the N > 1 replicas.  Its collectives (the barriers
+    around the timed region, the max over ranks) give up after
+    BENCH_DIST_TIMEOUT_S seconds (default 600), so a rank that died is
+    reported as an error on the others instead of a hang."""
+    import datetime
     import torch.distributed as dist
     if ws > 1 and not dist.is_initialized():
         os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
-        dist.init_process_group(backend=backend)
+        timeout = float(os.environ.get("BENCH_DIST_TIMEOUT_S", "600"))
+        dist.init_process_group(backend=backend, timeout=datetime.timedelta(seconds=timeout))
     return dist
 
 

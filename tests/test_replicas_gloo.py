@@ -53,3 +53,38 @@ def test_reference_arm_other_ranks_do_nothing(capsys, monkeypatch):
     args = type("A", (), dict(gpus=2, steps=1, warmup=3, workload="gpt2-small"))()
     assert bench.run_reference(args, 2, 1) == 0
     assert capsys.readouterr().out == ""
+
+
+def _worker_one_dies(rank, world, port, out):
+    sys.path.insert(0, ROOT)
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank), BENCH_DIST_TIMEOUT_S="5")
+    import bench
+    ws, r, local = bench.dist_env()
+    bench.init_dist(ws, "gloo")
+    bench.barrier(ws)                      # both ranks reach the first barrier
+    if rank == 1:
+        os._exit(3)                        # leaves between steps, nothing in flight
+    try:
+        bench.barrier(ws)                  # the survivor's next collective
+        out[rank] = "no error"
+    except Exception as e:                 # noqa: BLE001 -- any error is the point
+        out[rank] = type(e).__name__
+
+
+def test_dead_replica_is_reported_not_hung():
+    """A rank that exits between steps: the other rank's next barrier ends
+    with an error within the process-group timeout instead of waiting."""
+    world = 2
+    port = _free_port()
+    ctx = mp.get_context("spawn")
+    out = ctx.Manager().dict()
+    procs = [ctx.Process(target=_worker_one_dies, args=(r, world, port, out))
+             for r in range(world)]
+    for p in procs:
+        p.start()
+    procs[0].join(timeout=120)
+    procs[1].join(timeout=120)
+    assert procs[1].exitcode == 3
+    assert procs[0].exitcode == 0
+    assert out.get(0) not in (None, "no error")
