@@ -817,7 +817,7 @@ cudaError_t launch_staged_step(const MultiArgs& a, int n_ptrs, int mode, cudaStr
 // lane copies the tile's gradient (8 KB) and, after the first micro-step, its
 // accumulator (16 KB) into a ring of eight 24 KB stages, so that up to 192 KB
 // per SM are in flight whatever the consumers' registers hold.  Consumers add
-// in fp32 (exact adds, the same as the register kernel) and store the
+// in fp32 (one rounding per add, as the register kernel does) and store the
 // accumulator with 16-byte streaming stores.
 constexpr int kZ1Stages = 8;
 constexpr int kZ1GradBytes = kStagedTile * 2;                  // 8192

@@ -51,7 +51,7 @@ def test_zero1_against_oracle(oracle, numels, n_ranks, n_micro):
             zf.zero1_accumulate(u.grad_rows(), rows(acc), k == 1, u.layout)
             oracle.zero1_accumulate(bits(g), o_acc, first=(k == 1))
         torch.cuda.synchronize()
-        # the accumulators are exact element-wise fp32 sums: bit-identical
+        # the accumulators are element-wise fp32 sums, one rounding per add on both sides
         assert np.array_equal(acc.cpu().numpy().view(np.uint32), o_acc.view(np.uint32))
         zf.zero1_step(rows(acc), n_micro, *u.state_rows(), u.param_rows(), u.layout, hp)
         o_params = oracle.zero1_step(o_acc, o_master, o_m, o_v, n_micro=n_micro, lr=hp["lr"],
