@@ -3,8 +3,9 @@
  * FlatParameter.
  *
  * TEST INFRASTRUCTURE ONLY.  Only the test suite, the smoke check and the
- * benchmark's CPU-baseline leg may load this library.  The product path never
- * calls it, and it shares no code, header or constant with the CUDA library.
+ * benchmark's CPU-baseline and reference legs may load this library.  The
+ * product path never calls it, and it shares no code, header or constant with
+ * the CUDA library.
  *
  * Everything here is a plain scalar loop in the order the method is stated:
  * flatten/pad/shard, reduce-scatter by averaging, AdamW on each rank's shard
@@ -25,7 +26,15 @@
  *         then concatenation of the updated slices).
  *   [LA]  "FSDP", Latent Atlas (process-cxr.github.io) -- section 5.1
  *         (each unit's parameters flattened and split evenly over the ranks),
- *         section 8.2 (bf16 gradients handed to an fp32 master update).
+ *         section 8.2 (bf16 gradients handed to an fp32 master update),
+ *         section 9.5 (FSDP2 splits every parameter on its own).
+ *   [A03] "03 · FSDP (ZeRO-3): per-layer all-gather and reshard"
+ *         (llm-infra-atlas) -- section 4 (FSDP2: each parameter marked as
+ *         split along dim 0 over the data-parallel mesh).
+ *   Further sections used by single functions below: [L5] section 7.2
+ *   (per-parameter Shard(0)), [L5] section 3 on gradient accumulation
+ *   (ZeRO-1 accumulates locally and reduce-scatters once), [DZ] section 6
+ *   (a global gradient norm needs a reduction across shards).
  *
  * Readings where the pages leave a step open (each is also listed with the
  * design notes): decoupled weight decay theta*(1 - lr*wd) applied to the old
