@@ -386,7 +386,10 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
     const int lane = tid & 31;
     uint32_t it = 0;
     bool ok = true;
-    float sq_s = 0.0f, sq_c = 0.0f;   // compensated sum of squares (norm modes)
+    // compensated sums of squares (norm modes): packed pairs for whole groups,
+    // a scalar pair for the ragged end
+    float2 sq2_s = make_float2(0.0f, 0.0f), sq2_c = make_float2(0.0f, 0.0f);
+    float sq_s = 0.0f, sq_c = 0.0f;
     constexpr int RG = GradTraits<GT>::kRanksPerStage;
     for (int tile = blockIdx.x; tile < a.h.total_tiles && ok; tile += gridDim.x) {
         const TileGeom g = tile_geom<A, GT>(a, tile);
@@ -546,8 +549,19 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                 if constexpr (MODE == kModeRsAvgNorm) {
                     out[t] = __fdiv_rn(__fadd_rn(st[0][t], mean[t]), a.h.k.divisor);
                 }
-                if constexpr (ModeTraits<MODE>::kNorm) {
-                    if (t < nv) two_sum_add1(sq_s, sq_c, __fmul_rn(out[t], out[t]));
+            }
+            if constexpr (ModeTraits<MODE>::kNorm) {
+                if (nv == kVec) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const float2 o = make_float2(out[2 * q], out[2 * q + 1]);
+                        two_sum_add2(sq2_s, sq2_c, __fmul2_rn(o, o));
+                    }
+                } else {
+#pragma unroll
+                    for (int t = 0; t < kVec; ++t) {
+                        if (t < nv) two_sum_add1(sq_s, sq_c, __fmul_rn(out[t], out[t]));
+                    }
                 }
             }
             float* dst = state_ptr<MODE, A>(a, u, 0, g.r) + j;
@@ -626,7 +640,9 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
     if (lane == 0) atomicMin(consumed_min, it);
     if constexpr (ModeTraits<MODE>::kNorm) {
         // Warp sum of the threads' compensated sums, in double, fixed order.
-        double w = static_cast<double>(sq_s) + static_cast<double>(sq_c);
+        double w = static_cast<double>(sq2_s.x) + static_cast<double>(sq2_c.x) +
+                   static_cast<double>(sq2_s.y) + static_cast<double>(sq2_c.y) +
+                   static_cast<double>(sq_s) + static_cast<double>(sq_c);
 #pragma unroll
         for (int off = 16; off > 0; off >>= 1) w += __shfl_down_sync(0xFFFFFFFFu, w, off);
         if (lane == 0) warp_sq[tid >> 5] = w;
