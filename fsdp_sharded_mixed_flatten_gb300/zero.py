@@ -22,7 +22,9 @@ ERRORS = {-1: "ZERO_ERR_INVALID_ARG", -2: "ZERO_ERR_MISALIGNED", -3: "ZERO_ERR_S
 
 
 class ZeroError(RuntimeError):
-    """A non-OK status from the library (nothing was launched)."""
+    """A non-OK status from the library.  After an argument error
+    (ZERO_ERR_INVALID_ARG, ZERO_ERR_MISALIGNED, ZERO_ERR_SIZE) nothing was
+    queued; ZERO_ERR_CUDA may follow some launches or copies of the same call."""
 
     def __init__(self, code: int, message: str, func: str):
         self.code = code

@@ -39,8 +39,11 @@
  *   - Elements [P, P_pad) -- the tail padding -- of the gradients, master, m
  *     and v must be zero on entry; they then stay zero.
  *   - Non-finite gradients propagate as NaN/inf through the update.
- *   - On a non-OK return nothing was launched; zero_last_error() gives a
- *     message (per calling thread).
+ *   - Arguments are checked before anything is queued: after ZERO_ERR_INVALID_ARG,
+ *     ZERO_ERR_MISALIGNED or ZERO_ERR_SIZE nothing was launched or copied.  A
+ *     call that needs several launches or copies may return ZERO_ERR_CUDA after
+ *     queuing some of them.  zero_last_error() gives a message (per calling
+ *     thread).
  */
 #ifndef ZERO_FLAT_H
 #define ZERO_FLAT_H
