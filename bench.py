@@ -359,6 +359,48 @@ class ClipResident(Resident):
         return self.launches_per_step
 
 
+class Zero1Resident:
+    """The ZeRO-1 form of a step of K micro-batches on one unit: each rank
+    accumulates its full fp32 gradient locally (zero1_accumulate), then one
+    reduce-scatter of the accumulators with the update (zero1_step)."""
+
+    def __init__(self, w, n_micro=4):
+        import torch
+        from fsdp_sharded_mixed_flatten_gb300 import synthetic
+        from fsdp_sharded_mixed_flatten_gb300.buffers import FlatUnit, aligned_rows, rows
+        self.w = w
+        self.n_micro = n_micro
+        u = w.units[0]
+        self.fu = FlatUnit(u.numels, w.n_ranks)
+        self.fu.set_master_flat(synthetic.make_master_flat(u.numel, w.n_ranks, w.master_std,
+                                                           (w.name, u.name), device="cuda"))
+        for r in range(w.n_ranks):
+            synthetic.fill_grad_(self.fu.grads[r], self.fu.P, w.grad_std,
+                                 synthetic.seed_for(w.name, u.name, "grad", r),
+                                 w.outlier_frac, w.outlier_scale)
+        self.full_acc = aligned_rows(w.n_ranks, self.fu.P_pad, torch.float32, "cuda", 0)
+        self.acc_rows = rows(self.full_acc)
+        torch.cuda.synchronize()
+        self.units = [self.fu]
+        self.numel = self.fu.P
+        N, P_pad = w.n_ranks, self.fu.P_pad
+        self.bytes = P_pad * N * (6 + 10 * (n_micro - 1)) + P_pad * (4 * N + 26)
+        self.launches_per_step = n_micro + 1
+
+    def launch(self, step, hp_base, events=None):
+        import fsdp_sharded_mixed_flatten_gb300 as zf
+        fu = self.fu
+        if events is not None:
+            events[0][0].record()
+        for k in range(1, self.n_micro + 1):
+            zf.zero1_accumulate(fu.grad_rows(), self.acc_rows, k == 1, fu.layout)
+        zf.zero1_step(self.acc_rows, self.n_micro, *fu.state_rows(), fu.param_rows(), fu.layout,
+                      dict(hp_base, step=step))
+        if events is not None:
+            events[0][1].record()
+        return self.launches_per_step
+
+
 def timed_extra(res, steps, warmup, ws, device, hbm_peak):
     import gc
     import torch
@@ -693,16 +735,23 @@ def run_ours(args, ws, rank, local):
         return run_sweep(args, device, hbm_peak)
 
     w = synthetic.workload(args.workload)
-    res = Resident(w)
+    if args.variant == "clip":
+        res = ClipResident(w, max_norm=1.0)
+    elif args.variant == "per-param":
+        res = PerParamResident(w)
+    elif args.variant == "zero1":
+        res = Zero1Resident(w)
+    else:
+        res = Resident(w)
     clocks = ClockSampler(local)
     el, kern, launches, clock_info = time_resident(res, args.steps, args.warmup, ws, device,
                                                    clocks=clocks)
     value = ws * res.numel * args.steps / el
     achieved = res.bytes * args.steps / kern / 1e9
-    traffic = recorded_traffic(args.workload)
+    traffic = recorded_traffic(args.workload) if args.variant == "plain" else None
     n_launch = len(res.units)
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and args.variant == "plain":
         e2e_el, h2d, d2h = time_e2e(res, args.steps, args.warmup, ws, device)
         e2e = {"value": ws * res.numel * args.steps / e2e_el, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
@@ -736,7 +785,8 @@ def run_ours(args, ws, rank, local):
         "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
-        "config": {"workload": workload_label(args.workload), "n_ranks_logical": w.n_ranks,
+        "config": {"workload": workload_label(args.workload), "variant": args.variant,
+                   "n_ranks_logical": w.n_ranks,
                    "units": n_launch, "params": sum(u.numel for u in w.units),
                    "storage": "bf16 grads/params, fp32 master/m/v", "n_out": 1,
                    "bytes_per_step": step_bytes,
@@ -772,6 +822,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="gpt2-small",
                     help="gpt2-small | llama3-8b-layer | 7.5b | tiny | sweep:<P>:<N_d>")
+    ap.add_argument("--variant", default="plain", choices=["plain", "clip", "per-param", "zero1"],
+                    help="the timed step: plain (default), with global-norm clipping, as FSDP2 "
+                         "per-parameter units, or the ZeRO-1 form of 4 micro-steps (first unit)")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")

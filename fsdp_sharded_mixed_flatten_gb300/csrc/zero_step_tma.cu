@@ -675,18 +675,30 @@ staged_step_kernel(const __grid_constant__ A a) {
         issued = 0;
         consumed_min = 0xFFFFFFFFu;
         clip_coef = 1.0f;
-        if constexpr (MODE == kModeFromShard) {
-            // Total norm from the norm launches' partial sums, in a fixed order,
-            // so every CTA derives the same coefficient.
-            double total = 0.0;
-            for (int i = 0; i < a.h.n_partials; ++i) total += a.h.partials[i];
-            const double norm = sqrt(total);
-            const double coef = a.h.max_norm / (norm + 1e-6);
-            clip_coef = coef >= 1.0 ? 1.0f : static_cast<float>(coef);
-            if (blockIdx.x == 0 && a.h.norm_out != nullptr) *a.h.norm_out = static_cast<float>(norm);
-        }
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if constexpr (MODE == kModeFromShard) {
+        // Total norm from the norm launches' partial sums in a fixed order, so
+        // that every CTA derives the same coefficient: lane l of warp 0 adds
+        // slots l, l + 32, ... in turn, then a fixed shuffle tree (the lanes'
+        // loads overlap instead of one thread walking every slot).
+        if (threadIdx.x < 32) {
+            double t = 0.0;
+            for (int i = static_cast<int>(threadIdx.x); i < a.h.n_partials; i += 32) {
+                t += a.h.partials[i];
+            }
+#pragma unroll
+            for (int off = 16; off > 0; off >>= 1) t += __shfl_down_sync(0xFFFFFFFFu, t, off);
+            if (threadIdx.x == 0) {
+                const double norm = sqrt(t);
+                const double coef = a.h.max_norm / (norm + 1e-6);
+                clip_coef = coef >= 1.0 ? 1.0f : static_cast<float>(coef);
+                if (blockIdx.x == 0 && a.h.norm_out != nullptr) {
+                    *a.h.norm_out = static_cast<float>(norm);
+                }
+            }
+        }
     }
     __syncthreads();
     if (threadIdx.x >= kConsumers) {
