@@ -451,6 +451,32 @@ def time_resident(res, steps, warmup, ws, device, per_kernel=True, clocks=None):
     return elapsed_max, kern, launches, clock_info
 
 
+def time_graph(step_fn, n_steps, reps=5):
+    """Seconds per step of step_fn(t) replayed from a CUDA graph of n_steps
+    consecutive steps: the kernels run back to back, without the host's
+    per-call launch cost (tens of microseconds through Python and ctypes),
+    which would otherwise hide short kernels.  The graph fixes the step
+    number t of every captured call; the bytes and the work do not depend on
+    it.  The step is warmed up eagerly first (kernel attributes, caches)."""
+    import torch
+    step_fn(1)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for t in range(n_steps):
+            step_fn(2 + t)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    del g
+    return a.elapsed_time(b) / 1e3 / (reps * n_steps)
+
+
 def time_e2e(res, steps, warmup, ws, device):
     """The same step through the host-buffer entry point
     (zero_step_units_host): every step copies every unit's gradients from
@@ -651,6 +677,10 @@ def run_sweep(args, device, hbm_peak):
             torch.cuda.synchronize()
             un_el = a.elapsed_time(b) / 1e3
             un_bytes = fu.P_pad * (2 * n + 38)
+            # the same two steps replayed from CUDA graphs (no host launch cost)
+            n_graph = int(max(4, min(50, 5e9 // res.bytes)))
+            fused_g = time_graph(lambda t: res.launch(t, hp0), n_graph)
+            unfused_g = time_graph(unfused, n_graph)
             line = {"sweep": True, "P": P, "n_ranks": n, "P_pad": fu.P_pad, "S": fu.S,
                     "S_mod_8": fu.S % 8, "steps": steps,
                     "fused_bytes_per_step": res.bytes, "fused_ms": kern / steps * 1e3,
@@ -659,6 +689,11 @@ def run_sweep(args, device, hbm_peak):
                     "unfused_gbs": un_bytes * steps / un_el / 1e9,
                     "unfused_frac_of_measured_hbm": un_bytes * steps / un_el / 1e9 / hbm_peak,
                     "fused_speedup": un_el / kern,
+                    "graph_steps": n_graph,
+                    "fused_graph_ms": fused_g * 1e3,
+                    "fused_graph_frac_of_measured_hbm": res.bytes / fused_g / 1e9 / hbm_peak,
+                    "unfused_graph_ms": unfused_g * 1e3,
+                    "unfused_graph_frac_of_measured_hbm": un_bytes / unfused_g / 1e9 / hbm_peak,
                     "l2_resident": res.bytes < 4 * 129e6}
             print(json.dumps(line), flush=True)
             del res, fu, gsh, psh, master, m, v
