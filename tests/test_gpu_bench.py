@@ -1,0 +1,46 @@
+"""bench.py on the GPU: every variant prints one JSON line with the contract's
+keys, on small workloads (seconds each)."""
+import json
+import os
+import subprocess
+import sys
+
+import pytest
+import torch
+
+pytestmark = pytest.mark.gpu
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+KEYS = ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+        "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config", "roofline",
+        "cpu_baseline", "e2e", "gpu_launches", "clocks")
+
+
+def _run(*extra):
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    out = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "3",
+                          "--warmup", "3", "--no-extra", "--no-cpu", *extra],
+                         capture_output=True, text=True, timeout=900, cwd=ROOT,
+                         env=dict(os.environ, WORLD_SIZE="1", RANK="0", LOCAL_RANK="0"))
+    assert out.returncode == 0, out.stderr[-3000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    return json.loads(lines[0])
+
+
+def test_plain_with_host_leg():
+    d = _run("--workload", "tiny")
+    for k in KEYS:
+        assert k in d, k
+    assert d["value"] > 0 and d["gpu_launches"] == 3
+    assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0
+    assert d["roofline"]["bound"] == "hbm" and d["roofline"]["frac"] > 0
+
+
+@pytest.mark.parametrize("variant,workload", [("clip", "tiny"), ("per-param", "gpt2-small"),
+                                              ("zero1", "sweep:1048576:8")])
+def test_variants(variant, workload):
+    d = _run("--workload", workload, "--variant", variant, "--no-e2e")
+    assert d["config"]["variant"] == variant
+    assert d["value"] > 0 and d["roofline"]["achieved"] > 0 and d["gpu_launches"] > 0
