@@ -3,17 +3,23 @@
 
 One "step" is one optimizer step of the whole workload: for every FSDP unit,
 reduce-scatter by averaging of the N_d bf16 gradient buffers, AdamW on every
-rank's fp32 shard, bf16 cast and all-gather, i.e. one fused zero_step launch
-per unit.  Inputs (gradients, optimizer state) are synthetic and resident in
-HBM before the timed region; they are larger than L2, so no flush is needed.
+rank's fp32 shard, bf16 cast and all-gather -- one zero_step_units call,
+which packs the units into as few fused launches as it can.  Inputs
+(gradients, optimizer state) are synthetic and resident in HBM before the
+timed region; they are larger than L2, so no flush is needed.  The JSON line
+also carries the same step end to end through the host-buffer entry point
+(gradients copied in, parameters copied out every step), the roofline of the
+fused kernel, the CPU oracle's throughput, the clocks seen during the timed
+region and, unless --no-extra, the secondary workloads.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                  [--workload gpt2-small] [--no-extra]
+                  [--workload gpt2-small] [--variant plain|clip|per-param|zero1]
+                  [--no-extra] [--no-e2e] [--no-cpu] [--sweep [--sweep-sizes ...]]
 
 With N > 1 (launched under torch.distributed.run) every rank runs an
-independent replica of the workload on its own GPU (the path does not shard
-across GPUs); value = all ranks' parameters / max-over-ranks step time.
-`--impl reference` times the CPU oracle on a bounded sample instead.
+independent replica of the workload on its own GPU (replicas only: no
+collective on the data path); value = all ranks' parameters / max-over-ranks
+step time.  `--impl reference` times the CPU oracle on a bounded sample.
 """
 from __future__ import annotations
 
