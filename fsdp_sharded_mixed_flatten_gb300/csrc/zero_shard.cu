@@ -5,6 +5,10 @@
 //                       (section 3, step 3)
 //   flatten_kernel      per-tensor buffers <-> flat buffer / rank shards
 //                       (section 7.1: FlatParameter flatten + tail padding)
+//   zero1_accumulate_kernel  ZeRO-1 local fp32 accumulation of each rank's full
+//                       gradient with register loads (section 3, on gradient
+//                       accumulation); the default is the bulk-copy form in
+//                       zero_step_tma.cu
 #include "zero_kernels.cuh"
 
 namespace zf {

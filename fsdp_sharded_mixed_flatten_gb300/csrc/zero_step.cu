@@ -1,5 +1,8 @@
 // Reduce-scatter by averaging and the fused step of the sharded
-// mixed-precision FlatParameter update.
+// mixed-precision FlatParameter update, with direct (register) loads.  These
+// kernels run when ZERO_STEP_KERNEL=direct is set; by default the same
+// computation runs in the bulk-copy staged kernel of zero_step_tma.cu, with
+// bit-identical results.
 //
 // Method ("Lesson 5: ZeRO and FSDP (including the FSDP2 architecture)",
 // section 3): the ranks' gradients are reduce-scattered, each rank updates
