@@ -25,6 +25,10 @@ static_assert(zf::kMaxUnits == ZERO_UNITS_PER_LAUNCH && zf::kMaxPtrs == ZERO_POI
               "launch packing limits mismatch");
 static_assert(zf::kDeviceOk == ZERO_DEVICE_OK && zf::kDeviceTimeout == ZERO_DEVICE_TIMEOUT,
               "device status codes mismatch");
+// One unit always fits a launch: at most 5 pointers per rank (gradients,
+// master, m, v, accumulator) plus one per gathered output.
+static_assert(5 * ZERO_MAX_RANKS + ZERO_MAX_RANKS <= ZERO_POINTERS_PER_LAUNCH,
+              "a unit with the most ranks and outputs must fit one launch");
 
 namespace {
 
