@@ -19,7 +19,8 @@ region and, unless --no-extra, the secondary workloads.
 With N > 1 (launched under torch.distributed.run) every rank runs an
 independent replica of the workload on its own GPU (replicas only: no
 collective on the data path); value = all ranks' parameters / max-over-ranks
-step time.  `--impl reference` times the CPU oracle on a bounded sample.
+step time.  `--impl reference` times the CPU oracle on a bounded sample, one
+contiguous chunk per host core.
 """
 from __future__ import annotations
 
@@ -553,27 +554,82 @@ def _oracle_sample(E, workload="gpt2-small"):
     return w, synthetic.bf16_bits(g), master, np.zeros_like(master), np.zeros_like(master)
 
 
+def host_threads():
+    """Host cores this process may run on."""
+    try:
+        return max(1, len(os.sched_getaffinity(0)))
+    except AttributeError:
+        return max(1, os.cpu_count() or 1)
+
+
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else the machine)."""
+    import platform
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return platform.machine()
+
+
+class OracleRun:
+    """The oracle over one contiguous sample of E elements, cut into one
+    contiguous chunk per host thread.  The step is element-wise, so the chunks
+    are independent, and the oracle's C calls release the interpreter lock, so
+    the threads run in parallel."""
+
+    def __init__(self, E, threads, workload="gpt2-small"):
+        from concurrent.futures import ThreadPoolExecutor
+        import numpy as np
+        from fsdp_sharded_mixed_flatten_gb300 import synthetic
+        from oracle import Oracle
+        self.o, self.hp = Oracle(), synthetic.ADAMW_DEFAULTS
+        self.w, gb, master, m, v = _oracle_sample(E, workload)
+        self.E = E
+        edges = [(E * i // threads) & ~7 for i in range(threads)] + [E]
+        self.chunks = [(np.ascontiguousarray(gb[:, a:b]), master[a:b], m[a:b], v[a:b])
+                       for a, b in zip(edges, edges[1:]) if b > a]
+        self.pool = ThreadPoolExecutor(len(self.chunks))
+
+    def step(self, step):
+        for f in [self.pool.submit(self.o.sampled_step, *c, step=step, **self.hp)
+                  for c in self.chunks]:
+            f.result()
+
+    def close(self):
+        self.pool.shutdown()
+
+
 def cpu_baseline(seconds=8.0):
     """The CPU oracle as it stands, on a bounded contiguous sample of the
-    gpt2-small workload (first unit, all 8 ranks), single-threaded."""
-    from fsdp_sharded_mixed_flatten_gb300 import synthetic
-    from oracle import Oracle
-    o = Oracle()
-    E = 1 << 20
-    w, gb, master, m, v = _oracle_sample(E)
-    hp = synthetic.ADAMW_DEFAULTS
-    reps, t0, step = 0, time.perf_counter(), 0
+    gpt2-small workload (all 8 ranks): one chunk of 2^20 flat elements per
+    host core, the chunks stepped in parallel."""
+    threads = host_threads()
+    run = OracleRun(threads << 20, threads)
+    reps, step = 0, 0
+    t0 = time.perf_counter()
     while True:
         step += 1
-        o.sampled_step(gb, master, m, v, step=step, **hp)
+        run.step(step)
         reps += 1
         el = time.perf_counter() - t0
         if el >= seconds:
             break
-    return {"value": reps * E / el, "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": f"{E} contiguous flat elements x {w.n_ranks} ranks of the gpt2-small "
-                      f"workload, {reps} oracle steps in {el:.1f} s (single thread, double "
-                      f"arithmetic)"}
+    run.close()
+    return {"value": reps * run.E / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+            "cpu": cpu_model(),
+            "sample": f"{run.E} contiguous flat elements x {run.w.n_ranks} ranks of the gpt2-small "
+                      f"workload in {len(run.chunks)} chunks, one per thread; {reps} oracle steps "
+                      f"in {el:.1f} s (double arithmetic)"}
 
 
 # ----------------------------------------------------------------- arms ----
@@ -584,39 +640,38 @@ def run_reference(args, ws, rank, budget_s=90.0):
     that the whole run stays within about budget_s seconds."""
     if rank != 0:
         return 0
-    from fsdp_sharded_mixed_flatten_gb300 import synthetic
-    from oracle import Oracle
-    o = Oracle()
-    hp = synthetic.ADAMW_DEFAULTS
-    w, gb, master, m, v = _oracle_sample(1 << 16, args.workload)
+    threads = host_threads()
+    cal = OracleRun(threads << 14, threads, args.workload)
     t0 = time.perf_counter()
-    o.sampled_step(gb, master, m, v, step=1, **hp)
-    o.sampled_step(gb, master, m, v, step=2, **hp)
-    rate = 2 * (1 << 16) / (time.perf_counter() - t0)       # elements per second
+    cal.step(1)
+    cal.step(2)
+    rate = 2 * cal.E / (time.perf_counter() - t0)          # elements per second
+    cal.close()
     E = int(budget_s * rate / (args.steps + args.warmup))
-    E = max(1 << 10, min(1 << 20, E)) & ~7
-    w, gb, master, m, v = _oracle_sample(E, args.workload)
+    E = max(threads << 10, min(threads << 21, E)) & ~7
+    run = OracleRun(E, threads, args.workload)
     step = 0
     for _ in range(args.warmup):
         step += 1
-        o.sampled_step(gb, master, m, v, step=step, **hp)
+        run.step(step)
     t0 = time.perf_counter()
     for _ in range(args.steps):
         step += 1
-        o.sampled_step(gb, master, m, v, step=step, **hp)
+        run.step(step)
     el = time.perf_counter() - t0
+    run.close()
     value = E * args.steps / el
-    sample = (f"{E} contiguous flat elements x {w.n_ranks} ranks of the {args.workload} workload "
-              f"per step, {args.steps} timed oracle steps in {el:.1f} s (single thread, double "
-              f"arithmetic)")
+    sample = (f"{E} contiguous flat elements x {run.w.n_ranks} ranks of the {args.workload} "
+              f"workload per step in {len(run.chunks)} chunks, one per thread; {args.steps} "
+              f"timed oracle steps in {el:.1f} s (double arithmetic)")
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
             "config": {"workload": workload_label(args.workload), "sample": sample},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
-                             "sample": sample},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
+                             "cpu": cpu_model(), "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
