@@ -625,8 +625,10 @@ def cpu_baseline(seconds=8.0):
         if el >= seconds:
             break
     run.close()
-    return {"value": reps * run.E / el, "unit": UNIT, "cores": threads, "kind": "oracle",
+    rate = reps * run.E / el
+    return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
             "cpu": cpu_model(),
+            "extrapolated_full_step_s": sum(u.numel for u in run.w.units) / rate,
             "sample": f"{run.E} contiguous flat elements x {run.w.n_ranks} ranks of the gpt2-small "
                       f"workload in {len(run.chunks)} chunks, one per thread; {reps} oracle steps "
                       f"in {el:.1f} s (double arithmetic)"}
@@ -671,7 +673,9 @@ def run_reference(args, ws, rank, budget_s=90.0):
             "impl": "reference",
             "config": {"workload": workload_label(args.workload), "sample": sample},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
-                             "cpu": cpu_model(), "sample": sample},
+                             "cpu": cpu_model(), "sample": sample,
+                             "extrapolated_full_step_s":
+                                 sum(u.numel for u in run.w.units) / value},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
