@@ -139,6 +139,38 @@ int cuda_status(cudaError_t e, const char* what) {
     return ok();
 }
 
+// Host-side failure injection for tests of the error paths: while the
+// environment variable ZERO_INJECT_FAILURE is set, a CUDA call (a launch, a
+// copy, a stream ordering) whose label contains its value is not made, and
+// the entry point returns ZERO_ERR_CUDA as it would for a failed call.  Read
+// at every call.
+bool injected(const char* what) {
+    const char* v = std::getenv("ZERO_INJECT_FAILURE");
+    return v != nullptr && v[0] != '\0' && std::strstr(what, v) != nullptr;
+}
+
+// One CUDA call with its status converted, unless a test injects its failure.
+template <class F>
+int cuda_call(const char* what, F&& call) {
+    if (injected(what)) return fail(ZERO_ERR_CUDA, "%s: injected failure", what);
+    return cuda_status(call(), what);
+}
+
+// Label of a staged launch, by mode.
+const char* staged_label(int mode) {
+    switch (mode) {
+        case zf::kModePlain: return "staged launch: step";
+        case zf::kModeAccumFinal: return "staged launch: accumulated step";
+        case zf::kModeRsStore: return "staged launch: reduce-scatter";
+        case zf::kModeRsAdd: return "staged launch: reduce-scatter add";
+        case zf::kModeRsNorm: return "staged launch: clip norm pass";
+        case zf::kModeRsAvgNorm: return "staged launch: clip norm pass, last micro-step";
+        case zf::kModeFromShard: return "staged launch: clip update pass";
+        case zf::kModeMeanDiv: return "staged launch: ZeRO-1 step";
+        default: return "staged launch";
+    }
+}
+
 // Which fused / reduce-scatter kernel runs: the bulk-copy staged one
 // (default) or the direct-load one.  ZERO_STEP_KERNEL=direct selects the
 // latter (both compute bit-identical results); read at every call.
@@ -230,10 +262,10 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
             a.h.norm_out = nullptr;
         }
         if (clip == nullptr || !clip->dry_run) {
-            const cudaError_t e = mode == zf::kModeMeanDiv
-                                      ? zf::launch_staged_step_f32(a, np, stream)
-                                      : zf::launch_staged_step(a, np, mode, stream);
-            rc = cuda_status(e, "staged step launch");
+            rc = cuda_call(staged_label(mode), [&] {
+                return mode == zf::kModeMeanDiv ? zf::launch_staged_step_f32(a, np, stream)
+                                                : zf::launch_staged_step(a, np, mode, stream);
+            });
         }
         a.h.n_units = 0;
         a.h.total_tiles = 0;
@@ -300,8 +332,9 @@ int run_step_direct(const UnitView& u, int32_t micro_step, int32_t n_micro,
     const bool micro = u.accum != nullptr && n_micro > 1;
     if (micro && micro_step < n_micro) {
         for (int r = 0; r < n; ++r) args.accum[r] = u.accum[r];
-        return cuda_status(zf::launch_reduce_scatter<MAXR>(args, micro_step > 1 ? 1 : 0, stream),
-                           "reduce-scatter launch");
+        return cuda_call("reduce-scatter launch", [&] {
+            return zf::launch_reduce_scatter<MAXR>(args, micro_step > 1 ? 1 : 0, stream);
+        });
     }
     for (int r = 0; r < n; ++r) {
         args.master[r] = u.master[r];
@@ -312,9 +345,10 @@ int run_step_direct(const UnitView& u, int32_t micro_step, int32_t n_micro,
     for (int o = 0; o < u.n_out; ++o) args.out[o] = u.out[o];
     args.n_out = u.n_out;
     args.k = derive_consts(hp, micro ? static_cast<double>(n_micro) : 1.0);
-    return cuda_status(
-        zf::launch_fused_step<MAXR>(args, micro ? zf::kModeAccumFinal : zf::kModePlain, stream),
-        "fused step launch");
+    return cuda_call("fused step launch", [&] {
+        return zf::launch_fused_step<MAXR>(args, micro ? zf::kModeAccumFinal : zf::kModePlain,
+                                           stream);
+    });
 }
 
 // Validate one unit's arguments for zero_step / zero_step_units.
@@ -515,7 +549,8 @@ static int flatten_impl(const void* const* tensors, const int64_t* offsets, cons
         a.begin = offsets[t0];
         a.end = offsets[t1 - 1] + numels[t1 - 1];
         if (a.end > a.begin) {
-            if (int rc = cuda_status(zf::launch_flatten(a, elem_bytes, unflatten, st), "flatten launch"))
+            if (int rc = cuda_call("flatten launch",
+                                   [&] { return zf::launch_flatten(a, elem_bytes, unflatten, st); }))
                 return rc;
         }
     }
@@ -523,7 +558,9 @@ static int flatten_impl(const void* const* tensors, const int64_t* offsets, cons
         a.n_tensors = 0;
         a.begin = L->numel;
         a.end = L->numel_padded;
-        if (int rc = cuda_status(zf::launch_flatten(a, elem_bytes, 0, st), "padding launch")) return rc;
+        if (int rc = cuda_call("padding launch",
+                               [&] { return zf::launch_flatten(a, elem_bytes, 0, st); }))
+            return rc;
     }
     return ok();
 }
@@ -552,7 +589,8 @@ static int rs_impl(const uint16_t* const* grads, float* const* grad_shards, cons
         a.grads[k] = grads[k];
         a.accum[k] = grad_shards[k];
     }
-    return cuda_status(zf::launch_reduce_scatter<MAXR>(a, accumulate, st), "reduce-scatter launch");
+    return cuda_call("reduce-scatter launch",
+                     [&] { return zf::launch_reduce_scatter<MAXR>(a, accumulate, st); });
 }
 
 ZERO_API int zero_reduce_scatter(const uint16_t* const* grads, float* const* grad_shards,
@@ -594,7 +632,7 @@ static int adamw_impl(float* const* master, float* const* m, float* const* v,
         a.param_shards[r] = param_shards[r];
     }
     a.k = derive_consts(hp, static_cast<double>(grad_divisor));
-    return cuda_status(zf::launch_adamw_shards<MAXR>(a, st), "adamw launch");
+    return cuda_call("adamw launch", [&] { return zf::launch_adamw_shards<MAXR>(a, st); });
 }
 
 ZERO_API int zero_adamw_shard_step(float* const* master, float* const* m, float* const* v,
@@ -628,7 +666,7 @@ static int gather_impl(const uint16_t* const* param_shards, uint16_t* const* ful
     a.tiles_per_rank = tiles_per_rank(L);
     for (int r = 0; r < L->n_ranks; ++r) a.param_shards_in[r] = param_shards[r];
     for (int o = 0; o < n_out; ++o) a.out[o] = full[o];
-    return cuda_status(zf::launch_all_gather<MAXR>(a, st), "all-gather launch");
+    return cuda_call("all-gather launch", [&] { return zf::launch_all_gather<MAXR>(a, st); });
 }
 
 ZERO_API int zero_all_gather(const uint16_t* const* param_shards, uint16_t* const* full_params,
@@ -672,6 +710,7 @@ namespace {
 // An event recorded on `from` that `to` waits for; released at once (the
 // wait keeps what it needs).
 int order_streams(cudaStream_t from, cudaStream_t to, const char* what) {
+    if (injected(what)) return fail(ZERO_ERR_CUDA, "%s: injected failure", what);
     cudaEvent_t ev = nullptr;
     cudaError_t e = cudaEventCreateWithFlags(&ev, cudaEventDisableTiming);
     if (e == cudaSuccess) e = cudaEventRecord(ev, from);
@@ -743,6 +782,8 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
         if (int rc = order_streams(comp, h2d, "ordering the gradient copies")) return rc;
     }
     for (int i = 0; i < n_units; ++i) {
+        if (injected("gradient copy to the device"))
+            return fail(ZERO_ERR_CUDA, "gradient copy to the device: injected failure");
         const zero_unit_t& x = units[i];
         const int n = x.layout->n_ranks;
         const int64_t count = unpadded(x.layout) ? x.layout->numel : x.layout->numel_padded;
@@ -782,11 +823,11 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
             const zero_unit_t& x = units[i];
             if (host_params[i] == nullptr || x.n_out < 1 || x.full_params == nullptr) continue;
             const int64_t count = unpadded(x.layout) ? x.layout->numel : x.layout->numel_padded;
-            if (int rc = cuda_status(
-                    cudaMemcpyAsync(host_params[i], x.full_params[0],
-                                    static_cast<size_t>(count) * sizeof(uint16_t),
-                                    cudaMemcpyDeviceToHost, d2h),
-                    "parameter copy to the host"))
+            if (int rc = cuda_call("parameter copy to the host", [&] {
+                    return cudaMemcpyAsync(host_params[i], x.full_params[0],
+                                           static_cast<size_t>(count) * sizeof(uint16_t),
+                                           cudaMemcpyDeviceToHost, d2h);
+                }))
                 return rc;
         }
     }
@@ -1012,15 +1053,17 @@ ZERO_API int zero1_accumulate(const uint16_t* const* grads, float* const* full_a
     if (n <= 64) {
         static thread_local zf::StepArgs<64> a;
         go(a);
-        return cuda_status(staged ? zf::launch_zero1_accumulate_staged<64>(a, first, st)
-                                  : zf::launch_zero1_accumulate<64>(a, first, st),
-                           "accumulate launch");
+        return cuda_call("ZeRO-1 accumulate launch", [&] {
+            return staged ? zf::launch_zero1_accumulate_staged<64>(a, first, st)
+                          : zf::launch_zero1_accumulate<64>(a, first, st);
+        });
     }
     static thread_local zf::StepArgs<512> a;
     go(a);
-    return cuda_status(staged ? zf::launch_zero1_accumulate_staged<512>(a, first, st)
-                              : zf::launch_zero1_accumulate<512>(a, first, st),
-                       "accumulate launch");
+    return cuda_call("ZeRO-1 accumulate launch", [&] {
+        return staged ? zf::launch_zero1_accumulate_staged<512>(a, first, st)
+                      : zf::launch_zero1_accumulate<512>(a, first, st);
+    });
 }
 
 ZERO_API int zero1_step(const float* const* full_accum, int32_t n_micro, float* const* master,

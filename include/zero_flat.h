@@ -44,6 +44,13 @@
  *     call that needs several launches or copies may return ZERO_ERR_CUDA after
  *     queuing some of them.  zero_last_error() gives a message (per calling
  *     thread).
+ *   - Failure injection, for tests of callers' error paths: while the
+ *     environment variable ZERO_INJECT_FAILURE is set, every CUDA call the
+ *     library would make whose label contains its value (for example
+ *     "clip update pass", "staged launch", "gradient copy to the device") is
+ *     skipped and the entry point returns ZERO_ERR_CUDA, exactly as if that
+ *     call had failed; the calls before it in the same entry point are queued
+ *     as usual.  The variable is read at every call.
  */
 #ifndef ZERO_FLAT_H
 #define ZERO_FLAT_H

@@ -180,3 +180,28 @@ def test_host_step_rejects_bad_arguments_before_any_copy(lib):
         zf.zero_step_units_host([(good, bad, good, good, None, [0x90000], L)], (host_ok, None),
                                 1, 1, HP, 0, 0, 0, 0)
     assert ei.value.code == -2
+
+
+def test_injected_cuda_failure_is_reported(lib, monkeypatch):
+    """While ZERO_INJECT_FAILURE names a CUDA call, that call is skipped and
+    the entry point returns ZERO_ERR_CUDA with the call's label (the fake
+    addresses below are checked but never dereferenced)."""
+    off, L = zf.zero_flat_layout([100], 4)
+    good = [0x10000 * (i + 1) for i in range(4)]
+    for kernel, label in (("staged", "staged launch: step"), ("direct", "fused step launch")):
+        if kernel == "direct":
+            monkeypatch.setenv("ZERO_STEP_KERNEL", "direct")
+        monkeypatch.setenv("ZERO_INJECT_FAILURE", label)
+        with pytest.raises(zf.ZeroError) as ei:
+            zf.zero_step(good, good, good, good, None, 1, 1, [0x90000], L, HP, stream=0)
+        assert ei.value.code == -4
+        assert zf.zero_last_error() == label + ": injected failure"
+    monkeypatch.setenv("ZERO_INJECT_FAILURE", "all-gather")
+    with pytest.raises(zf.ZeroError) as ei:
+        zf.zero_all_gather(good, [0x90000], L, stream=0)
+    assert zf.zero_last_error() == "all-gather launch: injected failure"
+    # argument checks still come first
+    monkeypatch.setenv("ZERO_INJECT_FAILURE", "launch")
+    with pytest.raises(zf.ZeroError) as ei:
+        zf.zero_step(good, good, good, [0] * 4, None, 1, 1, [0x90000], L, HP, stream=0)
+    assert ei.value.code == -1
