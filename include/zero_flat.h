@@ -38,7 +38,12 @@
  *   - Offsets and sizes are element counts (int64_t).
  *   - Elements [P, P_pad) -- the tail padding -- of the gradients, master, m
  *     and v must be zero on entry; they then stay zero.
- *   - Non-finite gradients propagate as NaN/inf through the update.
+ *   - Non-finite gradients propagate through the update: an element whose
+ *     gradient is NaN or infinite on some rank averages to NaN (the error term
+ *     of the compensated rank sum is inf - inf), and its master, m and v
+ *     become NaN.  The clipped step reports a NaN norm then, and its NaN
+ *     coefficient makes every gradient NaN; a caller checks the norm to skip
+ *     such a step.
  *   - Arguments are checked before anything is queued: after ZERO_ERR_INVALID_ARG,
  *     ZERO_ERR_MISALIGNED or ZERO_ERR_SIZE nothing was launched or copied.  A
  *     call that needs several launches or copies may return ZERO_ERR_CUDA after

@@ -1,5 +1,7 @@
 """Global gradient-norm clipping across every shard and unit (the clipped
 multi-unit step) against the oracle, through the C ABI."""
+import math
+
 import numpy as np
 import pytest
 import torch
@@ -49,11 +51,14 @@ class ClipRun:
         return [(u.grad_rows(), *u.state_rows(), u.accum_rows(), u.param_rows(), u.layout)
                 for u in self.units]
 
-    def step(self, oracle, t, max_norm):
+    def step(self, oracle, t, max_norm, poison=None):
+        """poison: (unit, rank, element, value) written into that gradient."""
         hp = hp_at(t)
         for k in range(1, self.n_micro + 1):
             for i, (u, ou) in enumerate(zip(self.units, self.o_units)):
                 g = synthetic.make_grads(u.P, u.n_ranks, self.grad_std, (self.tag, i, t, k))
+                if poison is not None and poison[0] == i:
+                    g[poison[1], poison[2]] = poison[3]
                 u.grads.copy_(g.cuda())
                 ou["grads"] = bits(g)
             zf.zero_step_units_clip(self.tuples(), k, self.n_micro, hp, max_norm, self.workspace,
@@ -67,7 +72,8 @@ class ClipRun:
                 self.o_norms.append((norm, coef))
                 torch.cuda.synchronize()
                 got = float(self.norm.item())
-                assert abs(got - norm) <= 1e-6 * norm, (got, norm)
+                if poison is None:
+                    assert abs(got - norm) <= 1e-6 * norm, (got, norm)
 
     def compare(self):
         torch.cuda.synchronize()
@@ -154,4 +160,25 @@ def test_workspace_too_small_rejected():
     with pytest.raises(zf.ZeroError) as ei:
         zf.zero_step_units_clip(run.tuples(), 1, 1, hp_at(1), -1.0, run.workspace, run.ws_bytes)
     assert ei.value.code == -1
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
+@pytest.mark.parametrize("bad", ["nan", "inf"])
+def test_nonfinite_gradient_shows_in_the_norm(oracle, bad):
+    """A NaN or infinite gradient element makes the reported norm non-finite,
+    the caller's signal to skip the step.  (The compensated rank sum turns an
+    infinite value into NaN: its error term is inf - inf.)  With a NaN norm
+    the coefficient is NaN and poisons every gradient, as in the oracle and in
+    torch's clip_grad_norm_."""
+    run = ClipRun(SPECS[:2], "nonfinite-" + bad)
+    run.step(oracle, 1, 1.0, poison=(1, 3, 17, float(bad)))
+    got = float(run.norm.item())
+    assert math.isnan(got), got
+    o_norm = run.o_norms[0][0]
+    assert math.isnan(o_norm) if bad == "nan" else math.isinf(o_norm)
+    if bad == "nan":
+        for u, ou in zip(run.units, run.o_units):
+            for name in ("master", "m", "v"):
+                assert np.isnan(getattr(u, name).cpu().numpy()).all()
+                assert np.isnan(ou[name]).all()
     assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
