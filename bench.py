@@ -15,6 +15,7 @@ region and, unless --no-extra, the secondary workloads.
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                   [--workload gpt2-small] [--variant plain|clip|per-param|zero1]
                   [--no-extra] [--no-e2e] [--no-cpu] [--sweep [--sweep-sizes ...]]
+                  [--seed S]
 
 With N > 1 (launched under torch.distributed.run) every rank runs an
 independent replica of the workload on its own GPU (replicas only: no
@@ -671,7 +672,8 @@ def run_reference(args, ws, rank, budget_s=90.0):
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": workload_label(args.workload), "sample": sample},
+            "config": {"workload": workload_label(args.workload), "sample": sample,
+                       "seed": args.seed},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "cpu": cpu_model(), "sample": sample,
                              "extrapolated_full_step_s":
@@ -886,6 +888,7 @@ def run_ours(args, ws, rank, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
         "data": "synthetic",
         "config": {"workload": workload_label(args.workload), "variant": args.variant,
+                   "seed": args.seed,
                    "n_ranks_logical": w.n_ranks,
                    "units": n_launch, "params": sum(u.numel for u in w.units),
                    "storage": "bf16 grads/params, fp32 master/m/v", "n_out": 1,
@@ -931,7 +934,13 @@ def main():
     ap.add_argument("--sweep", action="store_true",
                     help="fused vs unfused over the flat-size x N_d sweep (JSON line per point)")
     ap.add_argument("--sweep-sizes", default="", help="comma-separated flat sizes for --sweep")
+    ap.add_argument("--seed", type=int, default=None,
+                    help="base seed of the synthetic draws (default: the library's fixed base)")
     args = ap.parse_args()
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    if args.seed is not None:
+        synthetic.BASE_SEED = args.seed
+    args.seed = synthetic.BASE_SEED
     if args.workload not in WORKLOAD_NAMES and not args.workload.startswith("sweep:"):
         ap.error(f"unknown workload {args.workload}")
     if args.warmup < 3:
