@@ -166,3 +166,88 @@ def test_unpadded_layout_rejected_where_unsupported():
     with pytest.raises(zf.ZeroError) as ei:
         zf.zero_all_gather(pu.state["master"], [pu.p_buf], pu.layout)
     assert ei.value.code == -1
+
+
+def _pair_units(tag):
+    """The same flat and per-parameter units twice, with equal seeded state."""
+    from fsdp_sharded_mixed_flatten_gb300.buffers import ParamUnit as PU
+    out = []
+    for _ in range(2):
+        units = []
+        for i, (d0, row) in enumerate([(33, 768), (5, 3), (4096, 1), (130, 2)]):
+            w = PU(d0, row, 8)
+            w.set_master_flat(synthetic.make_master_flat(w.numel, 1, 0.02, (tag, i)).cuda())
+            units.append(w)
+        for i, (numels, n) in enumerate([([300_001, 77], 8), ([65_536], 64)]):
+            f = FlatUnit(numels, n)
+            f.set_master_flat(synthetic.make_master_flat(f.P, n, 0.02, (tag, "flat", i)).cuda())
+            units.append(f)
+        out.append(units)
+    return out
+
+
+def _fill(units, tag, t):
+    gs = []
+    for i, u in enumerate(units):
+        n_ranks = u.n_ranks
+        numel = u.numel if hasattr(u, "sizes") else u.P
+        g = synthetic.make_grads(numel, n_ranks, 1e-2, (tag, i, t))[:, :u.grads.shape[1]]
+        u.grads.copy_(g.cuda())
+        gs.append(g.contiguous())
+    return gs
+
+
+def _tuple(u):
+    if hasattr(u, "unit_tuple"):
+        return u.unit_tuple()
+    return (u.grad_rows(), *u.state_rows(), None, u.param_rows(), u.layout)
+
+
+def _assert_same_state(a, b):
+    for x, y in zip(a, b):
+        for s, t in ((x.master, y.master), (x.m, y.m), (x.v, y.v)):
+            assert torch.equal(s.contiguous().view(torch.int32), t.contiguous().view(torch.int32))
+        assert torch.equal(x.params.contiguous().view(torch.int16),
+                           y.params.contiguous().view(torch.int16))
+
+
+def test_flat_and_per_parameter_units_in_one_call():
+    """FSDP1 flat units and FSDP2 per-parameter units stepped by one
+    zero_step_units call give the bits of one call per unit."""
+    a, b = _pair_units("mixed")
+    for t in (1, 2):
+        _fill(a, "mixed", t)
+        _fill(b, "mixed", t)
+        zf.zero_step_units([_tuple(u) for u in a], 1, 1, hp_at(t))
+        for u in b:
+            zf.zero_step_units([_tuple(u)], 1, 1, hp_at(t))
+    torch.cuda.synchronize()
+    _assert_same_state(a, b)
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
+def test_host_step_with_per_parameter_units():
+    """The host-buffer step moves exactly numel elements per per-parameter
+    unit (no padding) and gives the device step's bits."""
+    dev, host_side = _pair_units("host-pp")
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    comp = torch.cuda.current_stream()
+    for t in (1, 2):
+        gs = _fill(dev, "host-pp", t)
+        for u in host_side:
+            u.grads.zero_()
+        hg = [[g[k].clone().pin_memory() for k in range(g.shape[0])] for g in gs]
+        hp_out = [torch.full((u.params.shape[1] + 64,), SENTINEL,
+                             dtype=torch.bfloat16).pin_memory() for u in host_side]
+        zf.zero_step_units([_tuple(u) for u in dev], 1, 1, hp_at(t))
+        zf.zero_step_units_host([_tuple(u) for u in host_side], (hg, hp_out), 1, 1, hp_at(t), 0,
+                                h2d, comp, d2h)
+        d2h.synchronize()
+        torch.cuda.synchronize()
+        for u, hpo in zip(host_side, hp_out):
+            n = u.numel if hasattr(u, "sizes") else u.P_pad
+            assert torch.equal(hpo[:n].view(torch.int16), u.params[0, :n].cpu().view(torch.int16))
+            # nothing written past the parameter's (per-parameter) or padded (flat) length
+            assert bool(torch.all(hpo[u.params.shape[1]:] == SENTINEL))
+    _assert_same_state(dev, host_side)
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
