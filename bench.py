@@ -488,13 +488,14 @@ def time_graph(step_fn, n_steps, reps=5):
 def time_e2e(res, steps, warmup, ws, device):
     """The same step through the host-buffer entry point
     (zero_step_units_host): every step copies every unit's gradients from
-    pinned host memory (one 2D copy per unit) and the gathered bf16 parameters
-    back.  Two device gradient sets alternate, so a step's copies overlap the
+    pinned host memory and the gathered bf16 parameters back, through the SMs
+    (ZERO_HOST_SM_COPY: the copy engines stall periodically on this host
+    link).  Two device gradient sets alternate, so a step's copies overlap the
     previous step's update; the copies of a set wait for the step that last
     read it."""
     import torch
-    from fsdp_sharded_mixed_flatten_gb300 import (ZERO_HOST_GRADS_FREE, HostTables, synthetic,
-                                                  zero_step_units_host)
+    from fsdp_sharded_mixed_flatten_gb300 import (ZERO_HOST_GRADS_FREE, ZERO_HOST_SM_COPY,
+                                                  HostTables, synthetic, zero_step_units_host)
     from fsdp_sharded_mixed_flatten_gb300.buffers import aligned_rows
     from fsdp_sharded_mixed_flatten_gb300.zero import prepare_units
     hp = dict(synthetic.ADAMW_DEFAULTS)
@@ -517,7 +518,7 @@ def time_e2e(res, steps, warmup, ws, device):
             s_h2d.wait_event(done.pop(i - 2))    # the last step that read this set is done
         for k in range(1, res.n_micro + 1):
             zero_step_units_host(sets[i % 2], tables, k, res.n_micro, dict(hp, step=step),
-                                 ZERO_HOST_GRADS_FREE, s_h2d, comp, s_d2h)
+                                 ZERO_HOST_GRADS_FREE | ZERO_HOST_SM_COPY, s_h2d, comp, s_d2h)
         done[i] = comp.record_event()
 
     t = 1000
@@ -856,7 +857,9 @@ def run_ours(args, ws, rank, local):
     if not args.no_e2e and args.variant == "plain":
         e2e_el, h2d, d2h = time_e2e(res, args.steps, args.warmup, ws, device)
         e2e = {"value": ws * res.numel * args.steps / e2e_el, "unit": UNIT,
-               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h}
+               "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+               "transport": "SM loads/stores through the pinned buffers' device mapping "
+                            "(ZERO_HOST_SM_COPY)"}
     step_bytes = res.bytes
     del res
     import gc

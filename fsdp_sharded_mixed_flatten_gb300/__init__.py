@@ -12,7 +12,8 @@ from .zero import (ZERO_MAX_RANKS, zero1_accumulate, zero1_step, zero_param_layo
                    zero_flatten, zero_last_error, zero_reduce_scatter, zero_selftest_wait_timeout,
                    zero_shard_segments, zero_step, zero_step_units, zero_step_units_clip,
                    zero_step_units_clip_noalloc, zero_clip_workspace_bytes, zero_unflatten,
-                   zero_step_units_host, HostTables, ZERO_HOST_GRADS_FREE)
+                   zero_step_units_host, HostTables, ZERO_HOST_GRADS_FREE,
+                   ZERO_HOST_SM_COPY)
 
 __all__ = [
     "ZERO_MAX_RANKS", "zero1_accumulate", "zero1_step", "zero_param_layout", "zero_shard_numel", "ZeroAdamW", "ZeroError", "ZeroLayout", "load", "zero_abi_version",
@@ -21,5 +22,5 @@ __all__ = [
     "zero_last_error", "zero_reduce_scatter", "zero_selftest_wait_timeout",
     "zero_shard_segments", "zero_step", "zero_step_units", "zero_step_units_clip",
     "zero_clip_workspace_bytes", "zero_step_units_clip_noalloc",
-    "zero_unflatten", "zero_step_units_host", "HostTables", "ZERO_HOST_GRADS_FREE",
+    "zero_unflatten", "zero_step_units_host", "HostTables", "ZERO_HOST_GRADS_FREE", "ZERO_HOST_SM_COPY",
 ]

@@ -16,6 +16,7 @@
 #include <vector>
 
 #include "zero_flat.h"
+#include "zero_host.cuh"
 #include "zero_kernels.cuh"
 
 #define ZERO_API extern "C" __attribute__((visibility("default")))
@@ -743,6 +744,37 @@ bool evenly_spaced(const T* const* rows, int n, int64_t width, int64_t* pitch) {
     return true;
 }
 
+// The device address of pinned host memory at p (its device mapping), or
+// nullptr when p is not in pinned, mapped host memory.
+const void* host_mapping(const void* p) {
+    cudaPointerAttributes attr{};
+    if (cudaPointerGetAttributes(&attr, p) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return nullptr;
+    }
+    return attr.type == cudaMemoryTypeHost ? attr.devicePointer : nullptr;
+}
+
+// Segments for the SM copy kernel, launched in batches of kHostCopySegs.
+struct SmCopies {
+    zf::HostCopyArgs a;
+    cudaStream_t stream;
+    const char* what;
+
+    int add(const void* src, void* dst, int64_t bytes) {
+        a.src[a.n] = src;
+        a.dst[a.n] = dst;
+        a.bytes[a.n] = bytes;
+        return ++a.n == zf::kHostCopySegs ? flush() : ZERO_OK;
+    }
+    int flush() {
+        if (a.n == 0) return ZERO_OK;
+        const int rc = cuda_call(what, [&] { return zf::launch_host_copy(a, stream); });
+        a.n = 0;
+        return rc;
+    }
+};
+
 }  // namespace
 
 ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
@@ -753,7 +785,8 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
     if (units == nullptr || n_units < 1) return fail(ZERO_ERR_INVALID_ARG, "no units");
     if (n_units > 4096) return fail(ZERO_ERR_SIZE, "at most 4096 units per call");
     if (host_grads == nullptr) return fail(ZERO_ERR_INVALID_ARG, "host_grads is NULL");
-    if ((flags & ~ZERO_HOST_GRADS_FREE) != 0) return fail(ZERO_ERR_INVALID_ARG, "unknown flags");
+    if ((flags & ~(ZERO_HOST_GRADS_FREE | ZERO_HOST_SM_COPY)) != 0)
+        return fail(ZERO_ERR_INVALID_ARG, "unknown flags");
     for (int i = 0; i < n_units; ++i) {
         const zero_unit_t& x = units[i];
         if (x.layout == nullptr || x.grads == nullptr || host_grads[i] == nullptr)
@@ -781,6 +814,11 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
     if (!(flags & ZERO_HOST_GRADS_FREE)) {
         if (int rc = order_streams(comp, h2d, "ordering the gradient copies")) return rc;
     }
+    const bool sm_copy = (flags & ZERO_HOST_SM_COPY) != 0;
+    static thread_local SmCopies sm;
+    sm.a.n = 0;
+    sm.stream = h2d;
+    sm.what = "gradient copy to the device";
     for (int i = 0; i < n_units; ++i) {
         if (injected("gradient copy to the device"))
             return fail(ZERO_ERR_CUDA, "gradient copy to the device: injected failure");
@@ -791,7 +829,23 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
         int64_t dpitch = 0, spitch = 0;
         cudaError_t e = cudaSuccess;
         bool done = false;
-        if (n > 1 && evenly_spaced(x.grads, n, width, &dpitch) &&
+        if (sm_copy) {
+            // rows in pinned, mapped host memory on the 16-byte grid go through
+            // the SMs; any other row through a copy engine
+            for (int k = 0; k < n && e == cudaSuccess; ++k) {
+                const void* src = reinterpret_cast<uintptr_t>(host_grads[i][k]) % 16 == 0
+                                      ? host_mapping(host_grads[i][k])
+                                      : nullptr;
+                if (src != nullptr) {
+                    if (int rc = sm.add(src, const_cast<uint16_t*>(x.grads[k]), width)) return rc;
+                } else {
+                    e = cudaMemcpyAsync(const_cast<uint16_t*>(x.grads[k]), host_grads[i][k],
+                                        static_cast<size_t>(width), cudaMemcpyHostToDevice, h2d);
+                }
+            }
+            done = true;
+        }
+        if (!done && n > 1 && evenly_spaced(x.grads, n, width, &dpitch) &&
             evenly_spaced(host_grads[i], n, width, &spitch)) {
             // Evenly spaced rows need not lie in one allocation (separate
             // buffers can land at a regular stride): the runtime then rejects
@@ -814,22 +868,41 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
         }
         if (int rc = cuda_status(e, "gradient copy to the device")) return rc;
     }
+    if (int rc = sm.flush()) return rc;
     if (int rc = order_streams(h2d, comp, "ordering the step after the copies")) return rc;
+    if (host_params != nullptr) {
+        // the step overwrites the device parameters that earlier calls' copies
+        // to the host may still be reading
+        if (int rc = order_streams(d2h, comp, "ordering the step after earlier parameter copies"))
+            return rc;
+    }
     if (int rc = zero_step_units(units, n_units, micro_step, n_micro, hp, compute_stream)) return rc;
     const bool optimizer_runs = units[0].accum == nullptr || n_micro <= 1 || micro_step == n_micro;
     if (host_params != nullptr && optimizer_runs) {
         if (int rc = order_streams(comp, d2h, "ordering the parameter copies")) return rc;
+        sm.a.n = 0;
+        sm.stream = d2h;
+        sm.what = "parameter copy to the host";
         for (int i = 0; i < n_units; ++i) {
             const zero_unit_t& x = units[i];
             if (host_params[i] == nullptr || x.n_out < 1 || x.full_params == nullptr) continue;
             const int64_t count = unpadded(x.layout) ? x.layout->numel : x.layout->numel_padded;
+            const int64_t bytes = count * static_cast<int64_t>(sizeof(uint16_t));
+            void* dst = sm_copy && reinterpret_cast<uintptr_t>(host_params[i]) % 16 == 0
+                            ? const_cast<void*>(host_mapping(host_params[i]))
+                            : nullptr;
+            if (dst != nullptr) {
+                if (int rc = sm.add(x.full_params[0], dst, bytes)) return rc;
+                continue;
+            }
             if (int rc = cuda_call("parameter copy to the host", [&] {
                     return cudaMemcpyAsync(host_params[i], x.full_params[0],
-                                           static_cast<size_t>(count) * sizeof(uint16_t),
-                                           cudaMemcpyDeviceToHost, d2h);
+                                           static_cast<size_t>(bytes), cudaMemcpyDeviceToHost,
+                                           d2h);
                 }))
                 return rc;
         }
+        if (int rc = sm.flush()) return rc;
     }
     return ok();
 }

@@ -331,6 +331,7 @@ def zero_step_units(units, micro_step: int, n_micro: int, hp, stream=None):
 
 
 ZERO_HOST_GRADS_FREE = 1
+ZERO_HOST_SM_COPY = 2
 
 
 class HostTables:

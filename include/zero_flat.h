@@ -356,8 +356,18 @@ int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t
  *                     the flag the caller guarantees those buffers are free
  *                     (for instance it alternates two sets of gradient buffers
  *                     and orders h2d_stream itself), so that the next step's
- *                     copies overlap this step's update
- * The step itself runs on compute_stream once every copy has landed.  A unit
+ *                     copies overlap this step's update; ZERO_HOST_SM_COPY:
+ *                     rows in pinned, mapped host memory whose address is a
+ *                     multiple of 16 bytes move through the SMs (a copy kernel
+ *                     loading and storing through the host memory's device
+ *                     mapping, one CTA of 1024 threads per SM on h2d_stream
+ *                     and d2h_stream) instead of the copy engines; other rows still
+ *                     take the copy engines.  Measured on GB300: the same
+ *                     211 GB/s host-to-device, without the copy engines'
+ *                     periodic stalls.  The flags combine.
+ * The step itself runs on compute_stream once every copy has landed and once
+ * the parameter copies queued on d2h_stream by earlier calls are done (the
+ * step overwrites the device parameters they read).  A unit
  * whose rank rows are evenly spaced in both memories moves with one 2D copy
  * when the runtime accepts one (rows of separate allocations may be rejected),
  * otherwise with one copy per rank.  The call returns when everything is
@@ -368,6 +378,7 @@ int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t
  * ZERO_ERR_CUDA if a copy cannot be queued.
  */
 #define ZERO_HOST_GRADS_FREE 1
+#define ZERO_HOST_SM_COPY 2
 int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
                          const uint16_t* const* const* host_grads, uint16_t* const* host_params,
                          int32_t micro_step, int32_t n_micro, const zero_adamw_t* hp,

@@ -226,7 +226,8 @@ def test_flat_and_per_parameter_units_in_one_call():
     assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
 
 
-def test_host_step_with_per_parameter_units():
+@pytest.mark.parametrize("flags", [0, zf.ZERO_HOST_SM_COPY], ids=["copy_engines", "sm_copy"])
+def test_host_step_with_per_parameter_units(flags):
     """The host-buffer step moves exactly numel elements per per-parameter
     unit (no padding) and gives the device step's bits."""
     dev, host_side = _pair_units("host-pp")
@@ -240,8 +241,8 @@ def test_host_step_with_per_parameter_units():
         hp_out = [torch.full((u.params.shape[1] + 64,), SENTINEL,
                              dtype=torch.bfloat16).pin_memory() for u in host_side]
         zf.zero_step_units([_tuple(u) for u in dev], 1, 1, hp_at(t))
-        zf.zero_step_units_host([_tuple(u) for u in host_side], (hg, hp_out), 1, 1, hp_at(t), 0,
-                                h2d, comp, d2h)
+        zf.zero_step_units_host([_tuple(u) for u in host_side], (hg, hp_out), 1, 1, hp_at(t),
+                                flags, h2d, comp, d2h)
         d2h.synchronize()
         torch.cuda.synchronize()
         for u, hpo in zip(host_side, hp_out):

@@ -51,8 +51,13 @@ def assert_same(a, b):
 SPECS = [([4096 * 300 + 5, 1000], 8), ([999999], 3), ([77], 64)]
 
 
-@pytest.mark.parametrize("layout", ["strided", "rows"])
-def test_host_step_equals_device_step(layout):
+@pytest.mark.parametrize("flags", [0, zf.ZERO_HOST_SM_COPY], ids=["copy_engines", "sm_copy"])
+@pytest.mark.parametrize("layout", ["strided", "rows", "odd_offset"])
+def test_host_step_equals_device_step(layout, flags):
+    """Rows in one pinned block (the second unit's rows then sit off the
+    16-byte grid), in separate pinned buffers, or all at a 2-byte offset:
+    with ZERO_HOST_SM_COPY the aligned rows go through the SMs and the others
+    through the copy engines, with the same result."""
     dev, host_side = make_pair(SPECS, "host-" + layout)
     h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
     comp = torch.cuda.current_stream()
@@ -63,12 +68,18 @@ def test_host_step_equals_device_step(layout):
             if layout == "strided":      # one pinned block, rows evenly spaced
                 blk = g.pin_memory()
                 hg.append([blk[k] for k in range(u.n_ranks)])
-            else:                        # separate pinned rows (not evenly spaced)
+                hp_out.append(torch.empty(u.P_pad, dtype=torch.bfloat16).pin_memory())
+            elif layout == "rows":       # separate pinned rows (not evenly spaced)
                 hg.append([g[k].clone().pin_memory() for k in range(u.n_ranks)])
-            hp_out.append(torch.empty(u.P_pad, dtype=torch.bfloat16).pin_memory())
+                hp_out.append(torch.empty(u.P_pad, dtype=torch.bfloat16).pin_memory())
+            else:                        # every row and output 2 bytes past the grid
+                blk = torch.empty(u.n_ranks * u.P_pad + 1, dtype=torch.bfloat16).pin_memory()
+                blk[1:].view(u.n_ranks, u.P_pad).copy_(g)
+                hg.append([blk[1 + k * u.P_pad:1 + (k + 1) * u.P_pad] for k in range(u.n_ranks)])
+                hp_out.append(torch.empty(u.P_pad + 1, dtype=torch.bfloat16).pin_memory()[1:])
             dev[i].grads.copy_(g.cuda())
         zf.zero_step_units(tuples(dev), 1, 1, hp_at(t))
-        zf.zero_step_units_host(tuples(host_side), (hg, hp_out), 1, 1, hp_at(t), 0,
+        zf.zero_step_units_host(tuples(host_side), (hg, hp_out), 1, 1, hp_at(t), flags,
                                 h2d, comp, d2h)
         d2h.synchronize()
         torch.cuda.synchronize()
@@ -80,7 +91,8 @@ def test_host_step_equals_device_step(layout):
 
 def test_host_step_double_buffered_with_free_flag():
     """Two device gradient sets used alternately, the caller ordering the
-    copies after the step that last read the set (ZERO_HOST_GRADS_FREE)."""
+    copies after the step that last read the set (ZERO_HOST_GRADS_FREE), the
+    rows moved by the SMs (ZERO_HOST_SM_COPY)."""
     dev, host_side = make_pair(SPECS, "host-dbl")
     spare = [aligned_rows(u.n_ranks, u.P_pad, torch.bfloat16, "cuda", 0) for u in host_side]
     sets = [[u.grads for u in host_side], spare]
@@ -103,8 +115,8 @@ def test_host_step_double_buffered_with_free_flag():
             h2d.wait_event(done[t - 2])      # the step that last read this set is done
         units = [([cur[i][k] for k in range(u.n_ranks)], *u.state_rows(), None,
                   u.param_rows(), u.layout) for i, u in enumerate(host_side)]
-        zf.zero_step_units_host(units, (hg, hp_out), 1, 1, hp_at(t), zf.ZERO_HOST_GRADS_FREE,
-                                h2d, comp, d2h)
+        zf.zero_step_units_host(units, (hg, hp_out), 1, 1, hp_at(t),
+                                zf.ZERO_HOST_GRADS_FREE | zf.ZERO_HOST_SM_COPY, h2d, comp, d2h)
         done[t] = comp.record_event()
         d2h.synchronize()
         for u, hpo in zip(host_side, hp_out):
