@@ -350,7 +350,9 @@ int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t
  *                     allowed): when the optimizer runs (micro_step ==
  *                     n_micro), units[u].full_params[0] is copied into
  *                     host_params[u] on d2h_stream once the step is done
- *   flags             0, or ZERO_HOST_GRADS_FREE: by default the copies first
+ *   flags             0 or any of ZERO_HOST_GRADS_FREE, ZERO_HOST_SM_COPY
+ *                     (ZERO_ERR_INVALID_ARG for other bits).
+ *                     ZERO_HOST_GRADS_FREE: by default the copies first
  *                     wait for the work already queued on compute_stream,
  *                     which may still read the device gradient buffers; with
  *                     the flag the caller guarantees those buffers are free
