@@ -369,8 +369,8 @@ int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t
  *                     periodic stalls.  The flags combine.
  * The step itself runs on compute_stream once every copy has landed and once
  * the parameter copies queued on d2h_stream by earlier calls are done (the
- * step overwrites the device parameters they read).  A unit
- * whose rank rows are evenly spaced in both memories moves with one 2D copy
+ * step overwrites the device parameters they read).  On the copy engines a
+ * unit whose rank rows are evenly spaced in both memories moves with one 2D copy
  * when the runtime accepts one (rows of separate allocations may be rejected),
  * otherwise with one copy per rank.  The call returns when everything is
  * queued; synchronize d2h_stream (compute_stream if host_params is NULL)
