@@ -74,9 +74,10 @@ def test_clipped_step_failure_then_retry(monkeypatch, label):
     assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
 
 
+@pytest.mark.parametrize("flags", [0, zf.ZERO_HOST_SM_COPY], ids=["copy_engines", "sm_copy"])
 @pytest.mark.parametrize("label", ["gradient copy to the device", "staged launch: step",
                                    "parameter copy to the host"])
-def test_host_step_failure_then_retry(monkeypatch, label):
+def test_host_step_failure_then_retry(monkeypatch, label, flags):
     clean, failing = _units("inject-host"), _units("inject-host")
     host_g = [u.grads.cpu().pin_memory() for u in clean]
     host_p = [[torch.zeros(u.P_pad, dtype=torch.bfloat16).pin_memory() for u in clean]
@@ -85,7 +86,7 @@ def test_host_step_failure_then_retry(monkeypatch, label):
     def run(units, params):
         tables = HostTables([[g[k] for k in range(g.shape[0])] for g in host_g], params)
         s = torch.cuda.current_stream()
-        zf.zero_step_units_host(_tuples(units), tables, 1, 1, hp_at(1), 0, s, s, s)
+        zf.zero_step_units_host(_tuples(units), tables, 1, 1, hp_at(1), flags, s, s, s)
 
     run(clean, host_p[0])
     torch.cuda.synchronize()
