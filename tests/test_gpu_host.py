@@ -147,3 +147,28 @@ def test_host_step_accumulation_copies_params_at_the_last_micro_step():
     for u, hpo in zip(host_side, hp_out):
         assert torch.equal(hpo.view(torch.int16), u.params[0].cpu().view(torch.int16))
     assert_same(dev, host_side)
+
+
+def test_host_step_sm_copy_many_rows():
+    """More rows than one transfer launch holds (320 rows, 256 a launch), in
+    and out, through the SMs: the device step's bits."""
+    specs = [([1000 + 17 * i], 64) for i in range(5)]
+    dev, host_side = make_pair(specs, "host-many")
+    h2d, d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    comp = torch.cuda.current_stream()
+    for t in (1, 2):
+        hg, hp_out = [], []
+        for i, u in enumerate(host_side):
+            g = synthetic.make_grads(u.P, u.n_ranks, 1e-2, ("host-many", i, t))
+            hg.append([g[k].clone().pin_memory() for k in range(u.n_ranks)])
+            hp_out.append(torch.empty(u.P_pad, dtype=torch.bfloat16).pin_memory())
+            dev[i].grads.copy_(g.cuda())
+        zf.zero_step_units(tuples(dev), 1, 1, hp_at(t))
+        zf.zero_step_units_host(tuples(host_side), (hg, hp_out), 1, 1, hp_at(t),
+                                zf.ZERO_HOST_SM_COPY, h2d, comp, d2h)
+        d2h.synchronize()
+        torch.cuda.synchronize()
+        for u, hpo in zip(host_side, hp_out):
+            assert torch.equal(hpo.view(torch.int16), u.params[0].cpu().view(torch.int16))
+    assert_same(dev, host_side)
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
