@@ -876,7 +876,16 @@ ZERO_API int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
         if (int rc = order_streams(d2h, comp, "ordering the step after earlier parameter copies"))
             return rc;
     }
-    if (int rc = zero_step_units(units, n_units, micro_step, n_micro, hp, compute_stream)) return rc;
+    {
+        // with SM transfers the step leaves their SMs free, so that it runs
+        // beside the next step's gradient copy instead of behind it
+        struct Reserve {
+            explicit Reserve(int n) { zf::set_reserved_sms(n); }
+            ~Reserve() { zf::set_reserved_sms(0); }
+        } reserve(sm_copy ? zf::host_copy_ctas() : 0);
+        if (int rc = zero_step_units(units, n_units, micro_step, n_micro, hp, compute_stream))
+            return rc;
+    }
     const bool optimizer_runs = units[0].accum == nullptr || n_micro <= 1 || micro_step == n_micro;
     if (host_params != nullptr && optimizer_runs) {
         if (int rc = order_streams(comp, d2h, "ordering the parameter copies")) return rc;

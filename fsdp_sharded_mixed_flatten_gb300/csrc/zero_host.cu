@@ -4,10 +4,11 @@
 // reduce-scatter in and one all-gather out per step).  On GB300 the copy
 // engines' host-to-device copies come to stall for tens of milliseconds
 // every few hundred milliseconds once a host has run a few jobs, while SM
-// loads of the same pinned memory keep their 211 GB/s.  One CTA of 1024
-// threads per SM with two 16-byte loads in flight per thread (5 MB in flight
-// over the GPU) was the fastest of the shapes measured (128 to 1024 threads,
-// 1 to 8 loads each) for the host-buffer step's gradients.
+// loads of the same pinned memory keep their 211 GB/s.  CTAs of 1024 threads
+// with two 16-byte loads in flight per thread were the fastest of the shapes
+// measured (128 to 1024 threads, 1 to 8 loads each); on a third of the SMs,
+// beside a step kernel on the rest, they keep the link busy while the step
+// runs (16 to 48 SMs measured; 48 best).
 #include "zero_host.cuh"
 
 namespace zf {
@@ -57,11 +58,15 @@ int sm_count() {
 
 }  // namespace
 
+int host_copy_ctas() {
+    const int sms = sm_count();
+    return sms >= 3 ? sms / 3 : 1;
+}
+
 cudaError_t launch_host_copy(const HostCopyArgs& a, cudaStream_t stream) {
     if (a.n <= 0) return cudaSuccess;
-    const int sms = sm_count();
-    if (sms <= 0) return cudaErrorInvalidDevice;
-    host_copy_kernel<<<sms, kCopyThreads, 0, stream>>>(a);
+    if (sm_count() <= 0) return cudaErrorInvalidDevice;
+    host_copy_kernel<<<host_copy_ctas(), kCopyThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 

@@ -21,9 +21,17 @@ struct HostCopyArgs {
     int64_t bytes[kHostCopySegs];
 };
 
-// One CTA of 1024 threads per SM, at most 32 registers a thread.  Its CTAs
-// and those of the staged step kernel do not fit an SM together, so a step
-// queued behind a running copy starts as the copy's CTAs finish.
+// One CTA of 1024 threads per SM on a third of the SMs (host_copy_ctas), at
+// most 32 registers a thread.  Its CTAs and those of the staged step kernel
+// do not fit an SM together, so the host-buffer step sizes its step launches
+// for the other two thirds (set_reserved_sms) and the two run side by side.
 cudaError_t launch_host_copy(const HostCopyArgs& a, cudaStream_t stream);
+
+// CTAs (one per SM) of a transfer launch: a third of the SMs.
+int host_copy_ctas();
+
+// SMs that the calling thread's persistent step launches leave free (0: none);
+// defined with the grid sizing in zero_step.cu.
+void set_reserved_sms(int n);
 
 }  // namespace zf

@@ -21,6 +21,7 @@
 // aligned vectors that cover its 8 elements and realigns them in registers.
 #include <mutex>
 
+#include "zero_host.cuh"
 #include "zero_kernels.cuh"
 
 namespace zf {
@@ -200,6 +201,14 @@ reduce_scatter_kernel(const __grid_constant__ StepArgs<MAXR> a) {
     }
 }
 
+// SMs this thread's launches leave free for the host-buffer step's SM
+// transfers (set_reserved_sms): the persistent kernels then size their grids
+// for the remaining SMs, so that a step runs beside the next step's copy
+// instead of behind it.
+thread_local int t_reserved_sms = 0;
+
+void set_reserved_sms(int n) { t_reserved_sms = n > 0 ? n : 0; }
+
 // Resident CTAs per SM for (kernel, threads, smem) on a device, and the SM
 // count, looked up once and cached (the occupancy query is not free).
 int persistent_grid(const void* kernel, int threads, size_t smem, int64_t work_ctas) {
@@ -207,33 +216,34 @@ int persistent_grid(const void* kernel, int threads, size_t smem, int64_t work_c
         const void* kernel;
         int dev, threads;
         size_t smem;
-        int cap;
+        int sms, per_sm;
     };
     static std::mutex mu;
     static Entry cache[64];
     static int n_cached = 0;
     int dev = 0;
     cudaGetDevice(&dev);
-    int cap = 0;
+    int sms = 0, per_sm = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
         for (int i = 0; i < n_cached; ++i) {
             const Entry& e = cache[i];
             if (e.kernel == kernel && e.dev == dev && e.threads == threads && e.smem == smem) {
-                cap = e.cap;
+                sms = e.sms;
+                per_sm = e.per_sm;
                 break;
             }
         }
-        if (cap == 0) {
-            int sms = 0, per_sm = 0;
+        if (sms == 0) {
             cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
             cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
             if (sms < 1) sms = 1;
             if (per_sm < 1) per_sm = 1;
-            cap = sms * per_sm;
-            if (n_cached < 64) cache[n_cached++] = Entry{kernel, dev, threads, smem, cap};
+            if (n_cached < 64) cache[n_cached++] = Entry{kernel, dev, threads, smem, sms, per_sm};
         }
     }
+    const int usable = t_reserved_sms < sms ? sms - t_reserved_sms : 1;
+    const int64_t cap = static_cast<int64_t>(usable) * per_sm;
     const int64_t g = work_ctas < cap ? work_ctas : cap;
     return static_cast<int>(g < 1 ? 1 : g);
 }

@@ -362,11 +362,13 @@ int zero_clip_workspace_bytes(const zero_unit_t* units, int32_t n_units, int32_t
  *                     rows in pinned, mapped host memory whose address is a
  *                     multiple of 16 bytes move through the SMs (a copy kernel
  *                     loading and storing through the host memory's device
- *                     mapping, one CTA of 1024 threads per SM on h2d_stream
- *                     and d2h_stream) instead of the copy engines; other rows still
- *                     take the copy engines.  Measured on GB300: the same
- *                     211 GB/s host-to-device, without the copy engines'
- *                     periodic stalls.  The flags combine.
+ *                     mapping, CTAs of 1024 threads on a third of the SMs, on
+ *                     h2d_stream and d2h_stream) instead of the copy engines,
+ *                     and the step's launches size their grids for the other
+ *                     SMs, so that a step runs beside the next step's copy;
+ *                     other rows still take the copy engines.  Measured on
+ *                     GB300: the same 211 GB/s host-to-device, without the
+ *                     copy engines' periodic stalls.  The flags combine.
  * The step itself runs on compute_stream once every copy has landed and once
  * the parameter copies queued on d2h_stream by earlier calls are done (the
  * step overwrites the device parameters they read).  On the copy engines a
