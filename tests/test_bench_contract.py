@@ -28,3 +28,21 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
     assert d["config"]["workload"].startswith("gpt2-small")
+
+
+def test_threaded_oracle_baseline_computes_the_single_thread_result():
+    """The CPU baseline steps one contiguous chunk per thread; the step is
+    element-wise, so the chunks together must give the single-chunk bits."""
+    import numpy as np
+    sys.path.insert(0, ROOT)
+    import bench
+    runs = [bench.OracleRun(8 * 1024 + 40, t) for t in (1, 4)]
+    for r in runs:
+        r.step(1)
+        r.step(2)
+        r.close()
+    one = [np.concatenate([c[i] for c in runs[0].chunks]) for i in (1, 2, 3)]
+    four = [np.concatenate([c[i] for c in runs[1].chunks]) for i in (1, 2, 3)]
+    for x, y in zip(one, four):
+        assert x.shape == y.shape and np.array_equal(x.view(np.uint32), y.view(np.uint32))
+    assert len(runs[1].chunks) == 4
