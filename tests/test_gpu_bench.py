@@ -35,6 +35,12 @@ def test_plain_with_host_leg():
         assert k in d, k
     assert d["value"] > 0 and d["gpu_launches"] == 3
     assert d["e2e"]["value"] > 0 and d["e2e"]["h2d_bytes_per_step"] > 0
+    # the tiny workload: P = 4096*1024 + 1024 + 1000 = P_pad (divisible by N_d = 4);
+    # N_d bf16 gradient rows in, one bf16 parameter buffer out, every step
+    p_pad = 4196328
+    assert d["e2e"]["h2d_bytes_per_step"] == 4 * p_pad * 2
+    assert d["e2e"]["d2h_bytes_per_step"] == p_pad * 2
+    assert "ZERO_HOST_SM_COPY" in d["e2e"]["transport"]
     assert d["roofline"]["bound"] == "hbm" and d["roofline"]["frac"] > 0
 
 
