@@ -486,6 +486,34 @@ def check_clipped_units_step_vs_torch(o):
         assert np.all(np.abs(u["master"][0] - ref) <= 2.0 ** -20 * (np.abs(ref) + HP["lr"]))
 
 
+def check_clip_nonfinite_vs_torch(o):
+    """Non-finite gradients against torch.nn.utils.clip_grad_norm_ (no
+    error_if_nonfinite): a NaN gradient makes the norm and the coefficient NaN
+    and every clipped gradient NaN; an infinite one makes the norm infinite,
+    the coefficient 0, its own element NaN (inf * 0) and every other gradient
+    0."""
+    rng = np.random.default_rng(15)
+    for bad in (np.nan, np.inf):
+        parts = [rng.normal(0, 1e-2, n).astype(np.float32) for n in (17, 40)]
+        parts[1][5] = bad
+        params = [torch.nn.Parameter(torch.zeros(len(x))) for x in parts]
+        for p, x in zip(params, parts):
+            p.grad = torch.from_numpy(x.copy())
+        tnorm = float(torch.nn.utils.clip_grad_norm_(params, 1.0))
+        total = sum(o.sum_squares(x) for x in parts)
+        coef = o.clip_coefficient(total, 1.0)
+        if np.isnan(bad):
+            assert np.isnan(tnorm) and np.isnan(np.sqrt(total)) and np.isnan(coef)
+        else:
+            assert np.isinf(tnorm) and np.isinf(total) and coef == 0.0
+        for p, x in zip(params, parts):
+            y = x.copy()
+            o.scale(y, coef)
+            ref = p.grad.numpy()
+            assert np.array_equal(np.isnan(y), np.isnan(ref))
+            assert np.array_equal(y[~np.isnan(y)], ref[~np.isnan(ref)])
+
+
 def check_zero1_accumulation(o):
     """ZeRO-1 (accumulate full gradients locally, one reduce-scatter at the end):
     with one micro-step it is the plain step; with K equal micro-batches
@@ -594,6 +622,7 @@ ALL_CHECKS = [
     check_clip_coefficient_vs_torch,
     check_clip_closed_forms,
     check_clipped_units_step_vs_torch,
+    check_clip_nonfinite_vs_torch,
     check_zero1_accumulation,
     check_param_shard_bounds_vs_torch_chunk,
     check_param_sharded_step_equals_flat,

@@ -41,6 +41,7 @@ MUTANTS = {
     "clip_no_clamp": ("if (coef >= 1.0) {", "if (coef >= 1e300) {"),
     "clip_no_eps": ("double coef = max_norm / (norm + 1e-6);", "double coef = max_norm / norm;"),
     "clip_scale_ignored": ("g[i] = (float)((double)g[i] * (double)coef);", "g[i] = g[i];"),
+    "clip_nan_coefficient_ignored": ("if (coef >= 1.0) {", "if (!(coef < 1.0)) {"),
     "zero1_accum_not_reset": ("double prev = first ? 0.0 : (double)acc_full[idx];",
                               "double prev = (double)acc_full[idx];"),
     "zero1_no_micro_average": ("g[e] = (float)((double)mean / (double)n_micro);", "g[e] = mean;"),
