@@ -241,6 +241,7 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
     int np = 0;
     a.h.n_units = 0;
     a.h.total_tiles = 0;
+    a.h.grid = 0;
     a.h.k = k;
     auto flush = [&]() -> int {
         if (a.h.n_units == 0) return ZERO_OK;
@@ -252,10 +253,12 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
             a.h.max_norm = clip->max_norm;
             a.h.norm_out = clip->norm_out;
             if (mode == zf::kModeRsNorm || mode == zf::kModeRsAvgNorm) {
+                // The launch runs exactly `grid` CTAs, one partial sum each.
                 const int grid = zf::staged_grid(mode, a.h.total_tiles);
                 if (clip->slots_used + grid > clip->capacity && !clip->dry_run)
                     return fail(ZERO_ERR_SIZE, "clipping workspace too small: need %lld slots",
                                 (long long)(clip->slots_used + grid));
+                a.h.grid = grid;
                 clip->slots_used += grid;
             }
         } else {
@@ -270,6 +273,7 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
         }
         a.h.n_units = 0;
         a.h.total_tiles = 0;
+        a.h.grid = 0;
         np = 0;
         return rc;
     };
@@ -1030,21 +1034,33 @@ constexpr int kNoAllocMaxUnits = 256;
 
 // Device address of the scratch array for the current device.  Host code may
 // not use the array's name as a device address (it is a host-side stand-in),
-// so the address is looked up once per device with that device current.
-int noalloc_scratch(double** out) {
+// so the address is looked up with that device current.  The first call on a
+// device sets the address up.  Every later call made outside stream capture
+// looks it up again (cheap once the module is loaded), so that a context torn
+// down and recreated by cudaDeviceReset is given the new address rather than
+// a stale one; a call being captured uses the last address looked up, and a
+// capture on a device that has never been set up is refused.
+int noalloc_scratch(cudaStream_t stream, double** out) {
     int dev = -1;
     if (int rc = cuda_status(cudaGetDevice(&dev), "cudaGetDevice")) return rc;
     if (dev < 0 || dev >= kNoAllocMaxDevices)
         return fail(ZERO_ERR_SIZE, "device index %d beyond %d", dev, kNoAllocMaxDevices);
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (int rc = cuda_status(cudaStreamIsCapturing(stream, &cap), "cudaStreamIsCapturing"))
+        return rc;
     static std::mutex mu;
     static double* ptrs[kNoAllocMaxDevices] = {};
     std::lock_guard<std::mutex> lock(mu);
-    if (ptrs[dev] == nullptr) {
+    if (cap == cudaStreamCaptureStatusNone) {
         void* p = nullptr;
         if (int rc = cuda_status(cudaGetSymbolAddress(&p, g_noalloc_clip_partials),
                                  "cudaGetSymbolAddress(clipping scratch)"))
             return rc;
         ptrs[dev] = static_cast<double*>(p);
+    } else if (ptrs[dev] == nullptr) {
+        return fail(ZERO_ERR_INVALID_ARG,
+                    "the first zero_step_units_clip_noalloc call on a device must come before "
+                    "any stream capture (it sets up the scratch address)");
     }
     *out = ptrs[dev];
     return ZERO_OK;
@@ -1097,7 +1113,7 @@ ZERO_API int zero_step_units_clip_noalloc(const zero_unit_t* units, int32_t n_un
                     "(use zero_step_units_clip with a workspace)",
                     (long long)count.slots_used, ZERO_NOALLOC_CLIP_SLOTS);
     double* scratch = nullptr;
-    if (int rc = noalloc_scratch(&scratch)) return rc;
+    if (int rc = noalloc_scratch(st, &scratch)) return rc;
     ClipPlan plan;
     plan.partials = scratch;
     plan.capacity = ZERO_NOALLOC_CLIP_SLOTS;

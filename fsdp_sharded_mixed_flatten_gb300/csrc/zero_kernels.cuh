@@ -95,6 +95,7 @@ struct UnitDesc {
 struct MultiHeader {
     int32_t n_units;
     int32_t total_tiles;
+    int32_t grid;           // CTAs to launch; 0: the persistent grid for the kernel form
     AdamConsts k;
     // global gradient-norm clipping
     double* partials;       // per-CTA sums of squares of the averaged gradient
@@ -159,8 +160,9 @@ cudaError_t launch_zero1_accumulate(const StepArgs<MAXR>& a, int first, cudaStre
 // above runs under ZERO_STEP_KERNEL=direct).
 template <int MAXR>
 cudaError_t launch_zero1_accumulate_staged(const StepArgs<MAXR>& a, int first, cudaStream_t stream);
-// Grid a staged launch of `mode` over `total_tiles` tiles uses (persistent:
-// at most one CTA per SM); norm launches write this many partial sums.
+// Persistent grid for a staged launch over `total_tiles` tiles (at most one
+// CTA per SM).  A norm launch is given this many CTAs explicitly (h.grid) and
+// writes exactly this many partial sums.
 int staged_grid(int mode, int total_tiles);
 // One CTA waiting on a barrier that nothing completes (tests the bounded wait).
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);

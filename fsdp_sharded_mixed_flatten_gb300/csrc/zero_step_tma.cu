@@ -823,7 +823,11 @@ static cudaError_t launch_as(const A& a, cudaStream_t stream) {
         reinterpret_cast<const void*>(&staged_step_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>);
     cudaError_t e = prepare_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>(kfn);
     if (e != cudaSuccess) return e;
-    const int grid = persistent_grid(kfn, kTmaThreads, kStagedSmem, a.h.total_tiles);
+    // A norm launch runs exactly the CTAs whose partial-sum slots were
+    // counted (h.grid); the kernel has no inter-CTA dependence, so CTAs beyond
+    // the resident ones would only run in a later wave.
+    const int grid = a.h.grid > 0 ? a.h.grid
+                                  : persistent_grid(kfn, kTmaThreads, kStagedSmem, a.h.total_tiles);
     staged_step_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>
         <<<grid, kTmaThreads, kStagedSmem, stream>>>(a);
     return cudaGetLastError();

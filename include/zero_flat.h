@@ -398,9 +398,11 @@ int zero_step_units_host(const zero_unit_t* units, int32_t n_units,
  * sums live in a scratch array of ZERO_NOALLOC_CLIP_SLOTS doubles (32 KB) that
  * the library reserves on every GPU that loads it, until the process exits.
  * No counterpart on the pages: this is a deployment variant only.
- *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before any
- *     stream capture.
+ *   - The first call on a device sets up the array's device address (looked
+ *     up with that device current); make that first call before any stream
+ *     capture.  Later calls outside capture look the address up again, so a
+ *     cudaDeviceReset between calls is harmless; a call captured after a
+ *     reset, with no uncaptured call in between, would use the old address.
  *   - Every call shares the one array.  Each call writes every slot it later
  *     reads, so nothing needs clearing, but calls that overlap on the GPU
  *     (two streams at once) race on it: serialise them.
