@@ -266,6 +266,33 @@ class Oracle:
             raise ValueError("bad arguments to oracle_zero1_step")
         return full
 
+    def sampled_zero1_step(self, acc_at, master_at, m_at, v_at, *, n_micro, lr, beta1, beta2,
+                           eps, weight_decay, step):
+        """The ZeRO-1 step on gathered sample elements (element-wise, like
+        sampled_step): acc_at (n_ranks, n) float32 holds every rank's full fp32
+        accumulator at the sampled flat indices; master_at/m_at/v_at (n,) the
+        owning rank's state there, updated in place.  Returns the (n,) bf16 bits.
+        (Marshalling only: the columns are padded with zeros to a multiple of
+        n_ranks so that oracle_zero1_step sees a (n_ranks, S) layout; the step is
+        element-wise, so which rank a column is filed under does not matter.)"""
+        acc_at = _f32(acc_at)
+        n_ranks, n = acc_at.shape
+        n_pad = -(-max(n, 1) // n_ranks) * n_ranks
+        acc = np.zeros((n_ranks, n_pad), dtype=np.float32)
+        acc[:, :n] = acc_at
+        st = [np.zeros(n_pad, dtype=np.float32) for _ in range(3)]
+        for dst, src in zip(st, (master_at, m_at, v_at)):
+            dst[:n] = src
+        full = np.empty(n_pad, dtype=np.uint16)
+        rc = self.lib.oracle_zero1_step(_ptr(acc), n_ranks, n_pad // n_ranks, int(n_micro),
+                                        _ptr(st[0]), _ptr(st[1]), _ptr(st[2]), _ptr(full), lr,
+                                        beta1, beta2, eps, weight_decay, int(step))
+        if rc != 0:
+            raise ValueError("bad arguments to oracle_zero1_step")
+        for dst, src in zip((master_at, m_at, v_at), st):
+            dst[:] = src[:n]
+        return full[:n].copy()
+
     # -- gradient clipping ----------------------------------------------
     def sum_squares(self, g) -> float:
         g = _f32(g)

@@ -106,3 +106,59 @@ class Case:
             parity.check_bf16_is_rounded_master(g_params[o], flat_master)
         assert np.all(g_params[:, self.P:] == 0), "padding of the parameters is not zero"
         assert np.all(g_master.reshape(-1)[self.P:] == 0) if self.P_pad > self.P else True
+
+
+def sample_indices(unit: FlatUnit, n_random: int, seed: int) -> np.ndarray:
+    """Flat indices of a unit the oracle follows in the full-size tests: random
+    ones plus every shard boundary, the first and last element, every tensor
+    boundary and the whole padded tail."""
+    rng = np.random.default_rng(seed)
+    S, P, P_pad = unit.S, unit.P, unit.P_pad
+    idx = set(rng.integers(0, P, size=n_random).tolist())
+    for r in range(unit.n_ranks):
+        for d in (0, 1, 2, 7, 8, S - 2, S - 1):
+            if 0 <= d < S:
+                idx.add(r * S + d)
+    for off, n in zip(unit.offsets, unit.numels):
+        for e in (off - 1, off, off + n - 1):
+            if 0 <= e < P_pad:
+                idx.add(e)
+    idx.update(range(P, P_pad))
+    idx.update((0, P - 1))
+    return np.array(sorted(idx), dtype=np.int64)
+
+
+class Sample:
+    """The oracle's copy of one unit's state at sampled flat indices (the step
+    is element-wise, so these elements can be followed exactly)."""
+
+    def __init__(self, unit: FlatUnit, idx: np.ndarray, master_flat: torch.Tensor, n_micro=1):
+        self.unit = unit
+        self.idx = idx
+        self.idx_t = torch.from_numpy(idx).to(master_flat.device)
+        self.r_t, self.i_t = self.idx_t // unit.S, self.idx_t % unit.S
+        self.master = master_flat[self.idx_t].cpu().numpy().copy()
+        self.m = np.zeros_like(self.master)
+        self.v = np.zeros_like(self.master)
+        self.acc = np.zeros_like(self.master) if n_micro > 1 else None
+        self.params = None
+
+    def grads_at(self) -> np.ndarray:
+        """Every rank's gradient at the sampled indices, (n_ranks, n) bf16 bits."""
+        return bits(self.unit.grads[:, self.idx_t].cpu())
+
+    def gpu_state(self):
+        u = self.unit
+        return (u.master[self.r_t, self.i_t].cpu().numpy(), u.m[self.r_t, self.i_t].cpu().numpy(),
+                u.v[self.r_t, self.i_t].cpu().numpy(), bits(u.params[0, self.idx_t].cpu()))
+
+    def compare(self):
+        import parity
+        g_master, g_m, g_v, g_p = self.gpu_state()
+        parity.check_state("master", g_master, self.master)
+        parity.check_state("m", g_m, self.m)
+        parity.check_state("v", g_v, self.v)
+        parity.check_bf16(g_p, self.params)
+        parity.check_bf16_is_rounded_master(g_p, g_master)
+        pad = self.idx >= self.unit.P
+        assert np.all(g_p[pad] == 0) and np.all(g_master[pad] == 0)

@@ -553,6 +553,42 @@ def check_zero1_accumulation(o):
     assert np.array_equal(ma.view(np.uint32), mb.view(np.uint32))
 
 
+def check_sampled_steps_equal_full_steps(o):
+    """The sampled forms the full-size GPU tests use (the step on a subset of
+    flat elements) give, on every element, the bits of the full step: the plain
+    step (sampled_step vs zero_step, 3 steps with padding) and the ZeRO-1 step
+    (sampled_zero1_step vs zero1_step, K = 3)."""
+    rng = np.random.default_rng(15)
+    n_ranks, P = 5, 83
+    grads, theta, S = _random_state(rng, n_ranks, P)
+    P_pad = n_ranks * S
+    ma, m1, v1 = (theta.reshape(n_ranks, S).copy(), np.zeros((n_ranks, S), np.float32),
+                  np.zeros((n_ranks, S), np.float32))
+    sm, s_m, s_v = theta.copy(), np.zeros(P_pad, np.float32), np.zeros(P_pad, np.float32)
+    for t in (1, 2, 3):
+        full = o.zero_step(grads, ma, m1, v1, step=t, **HP)
+        part = o.sampled_step(grads, sm, s_m, s_v, step=t, **HP)
+        assert np.array_equal(full, part)
+        assert np.array_equal(ma.reshape(-1).view(np.uint32), sm.view(np.uint32))
+        assert np.array_equal(v1.reshape(-1).view(np.uint32), s_v.view(np.uint32))
+    K = 3
+    acc = np.zeros((n_ranks, P_pad), np.float32)
+    for k in range(1, K + 1):
+        g = random_bf16(rng, (n_ranks, P_pad), 1e-2)
+        o.zero1_accumulate(g, acc, first=(k == 1))
+    mb, m2, v2 = (theta.reshape(n_ranks, S).copy(), np.zeros((n_ranks, S), np.float32),
+                  np.zeros((n_ranks, S), np.float32))
+    full = o.zero1_step(acc, mb, m2, v2, n_micro=K, step=1, **HP)
+    cols = np.array([0, 1, 7, S - 1, S, 2 * S + 3, P_pad - 1])
+    sm, s_m, s_v = (theta[cols].copy(), np.zeros(cols.size, np.float32),
+                    np.zeros(cols.size, np.float32))
+    part = o.sampled_zero1_step(np.ascontiguousarray(acc[:, cols]), sm, s_m, s_v, n_micro=K,
+                                step=1, **HP)
+    assert np.array_equal(full[cols], part)
+    assert np.array_equal(mb.reshape(-1)[cols].view(np.uint32), sm.view(np.uint32))
+    assert np.array_equal(m2.reshape(-1)[cols].view(np.uint32), s_m.view(np.uint32))
+
+
 def check_param_shard_bounds_vs_torch_chunk(o):
     """Per-parameter Shard(0): each rank's rows are the chunk torch.chunk gives
     (a library routine), in order, with no padding; chunks past the end are empty."""
@@ -624,6 +660,7 @@ ALL_CHECKS = [
     check_clipped_units_step_vs_torch,
     check_clip_nonfinite_vs_torch,
     check_zero1_accumulation,
+    check_sampled_steps_equal_full_steps,
     check_param_shard_bounds_vs_torch_chunk,
     check_param_sharded_step_equals_flat,
 ]

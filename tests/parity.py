@@ -18,7 +18,19 @@ Derivation (restated in the design notes):
 """
 from __future__ import annotations
 
+import os
+
 import numpy as np
+
+# Margins of every check made in this process, one record per call: printed
+# as a table at the end of a pytest session (and written as JSON lines to
+# $PARITY_MARGINS_JSON when that is set).
+MARGINS = []
+
+
+def _record(kind, what, **fields):
+    test = os.environ.get("PYTEST_CURRENT_TEST", "").split(" ")[0]
+    MARGINS.append(dict(test=test, kind=kind, what=what, **fields))
 
 
 def _fmt(idx, got, ref):
@@ -29,13 +41,20 @@ def check_mean(got, ref, abs_mean_x, what="mean"):
     got = np.asarray(got, dtype=np.float64)
     ref = np.asarray(ref, dtype=np.float64)
     tol = 2.0 ** -23 * np.abs(ref) + 2.0 ** -35 * np.asarray(abs_mean_x, dtype=np.float64)
-    bad = np.nonzero(np.abs(got - ref) > tol)[0]
+    d = np.abs(got - ref)
+    _record("mean", what, n=int(ref.size),
+            max_over_tol=float(np.max(d / np.maximum(tol, 1e-300))) if ref.size else 0.0,
+            max_f32_ulp=_max_f32_ulp(got, ref), exact=_exact_fraction(got, ref))
+    bad = np.nonzero(d > tol)[0]
     assert bad.size == 0, f"{what}: {bad.size} elements out of tolerance; " + \
         _fmt(bad[0], got[bad[0]], ref[bad[0]])
 
 
 def check_state(name, got, ref, floor_scale=None):
-    """master: |d| <= 1e-6|ref| + 1e-7; m, v: |d| <= 1e-6|ref| + 1e-7*max|ref|."""
+    """master: |d| <= 1e-6|ref| + 1e-7; m, v: |d| <= 1e-6|ref| + 1e-7*max|ref|.
+    Records the largest relative error, the largest distance in fp32 ulps, the
+    bit-identical fraction and how many elements pass only through the
+    absolute floor."""
     got = np.asarray(got, dtype=np.float64).ravel()
     ref = np.asarray(ref, dtype=np.float64).ravel()
     if name == "master":
@@ -45,10 +64,36 @@ def check_state(name, got, ref, floor_scale=None):
         floor = 1e-7 * scale
     tol = 1e-6 * np.abs(ref) + floor
     d = np.abs(got - ref)
+    nz = ref != 0
+    _record("state", name, n=int(ref.size),
+            max_rel=float(np.max(d[nz] / np.abs(ref[nz]))) if nz.any() else 0.0,
+            max_over_tol=float(np.max(d / np.maximum(tol, 1e-300))) if ref.size else 0.0,
+            floor_only=int(np.count_nonzero((d > 1e-6 * np.abs(ref)) & (d <= tol))),
+            max_f32_ulp=_max_f32_ulp(got, ref), exact=_exact_fraction(got, ref))
     bad = np.nonzero(~(d <= tol))[0]
     assert bad.size == 0, f"{name}: {bad.size}/{ref.size} out of tolerance; " + \
         _fmt(bad[0], got[bad[0]], ref[bad[0]])
     return float(np.max(d / np.maximum(tol, 1e-300))) if ref.size else 0.0
+
+
+def _f32_ordered(x):
+    """fp32 values as integers in value order (adjacent floats differ by 1)."""
+    b = np.asarray(x, dtype=np.float32).view(np.int32).astype(np.int64)
+    return np.where(b < 0, -(b & 0x7FFFFFFF), b)
+
+
+def _max_f32_ulp(got, ref):
+    if np.size(ref) == 0:
+        return 0
+    return int(np.max(np.abs(_f32_ordered(got) - _f32_ordered(ref))))
+
+
+def _exact_fraction(got, ref):
+    if np.size(ref) == 0:
+        return 1.0
+    g = np.asarray(got, dtype=np.float32)
+    r = np.asarray(ref, dtype=np.float32)
+    return float(np.mean(g.view(np.int32) == r.view(np.int32)))
 
 
 def bf16_ordered(bits):
@@ -74,7 +119,13 @@ def check_bf16(got_bits, ref_bits, what="params", min_exact=0.999):
     got_bits = np.asarray(got_bits)
     ref_bits = np.asarray(ref_bits)
     d = np.abs(bf16_value(got_bits) - bf16_value(ref_bits))
-    tol = bf16_ulp(ref_bits) + 1e-7
+    ulp = bf16_ulp(ref_bits)
+    tol = ulp + 1e-7
+    _record("bf16", what, n=int(ref_bits.size),
+            max_ulp=int(np.max(np.abs(bf16_ordered(got_bits) - bf16_ordered(ref_bits))))
+            if got_bits.size else 0,
+            floor_only=int(np.count_nonzero((d > ulp) & (d <= tol))),
+            exact=float(np.mean(got_bits == ref_bits)) if got_bits.size else 1.0)
     bad = np.nonzero(d > tol)[0]
     assert bad.size == 0, f"{what}: {bad.size} bf16 values out of tolerance; " + \
         _fmt(bad[0], int(got_bits[bad[0]]), int(ref_bits[bad[0]]))

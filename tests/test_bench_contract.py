@@ -27,7 +27,9 @@ def test_reference_arm_json_line():
     assert d["value"] > 0 and d["ms_per_step"] > 0 and d["higher_is_better"] is True
     assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
     assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["d2h_bytes_per_step"] == 0
-    assert d["config"]["workload"].startswith("gpt2-small")
+    # the default workload: the pages' 7.5B model as 32 units over 64 logical ranks
+    assert d["config"]["workload"] == "7.5B-32units-Nd64"
+    assert "x 64 ranks of the 7.5b workload" in d["cpu_baseline"]["sample"]
 
 
 def test_threaded_oracle_baseline_computes_the_single_thread_result():

@@ -50,3 +50,22 @@ def test_variants(variant, workload):
     d = _run("--workload", workload, "--variant", variant, "--no-e2e")
     assert d["config"]["variant"] == variant
     assert d["value"] > 0 and d["roofline"]["achieved"] > 0 and d["gpu_launches"] > 0
+
+
+def test_streamed_host_leg_byte_counts():
+    """The 7.5B model's end-to-end leg (gradients streamed unit by unit from
+    host memory through two device buffers) on a small stand-in: 4 units of
+    100,003 elements sharing one gradient buffer, N_d = 8."""
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    sys.path.insert(0, ROOT)
+    import bench
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    w = synthetic.Workload("streamed-test", tuple(synthetic.Unit(f"u{i}", (100003,))
+                                                  for i in range(4)), 8, 1e-3)
+    res = bench.Resident(w, shared_grads=True)
+    assert all(fu.grads is res.units[0].grads for fu in res.units)
+    p_pad = synthetic.padded(100003, 8)
+    el, h2d, d2h = bench.time_e2e_streamed(res, 2, 1, 1, torch.device("cuda", 0))
+    assert el > 0
+    assert h2d == 4 * 8 * p_pad * 2 and d2h == 4 * p_pad * 2

@@ -59,10 +59,11 @@ CASES = [
 ]
 
 
-@pytest.fixture(params=["staged", "direct"])
+@pytest.fixture(params=["staged", "direct", "unfused"])
 def kernel(request, monkeypatch):
-    """Run a test with the bulk-copy staged kernels (default) and again with
-    the direct-load kernels."""
+    """Run a test with the bulk-copy staged fused kernel (default), again with
+    the direct-load kernels, and again through the unfused entry points
+    (zero_reduce_scatter, zero_adamw_shard_step, zero_all_gather)."""
     if request.param == "direct":
         monkeypatch.setenv("ZERO_STEP_KERNEL", "direct")
     else:
@@ -74,7 +75,8 @@ def kernel(request, monkeypatch):
 @pytest.mark.parametrize("name,numels,n_ranks,n_out,n_micro,steps", CASES,
                          ids=[c[0] for c in CASES])
 def test_small_cases(oracle, kernel, name, numels, n_ranks, n_out, n_micro, steps):
-    c = Case(numels, n_ranks, n_out=n_out, n_micro=n_micro, tag=name)
+    c = Case(numels, n_ranks, n_out=n_out, n_micro=n_micro, tag=name,
+             path="unfused" if kernel == "unfused" else "fused")
     for t in range(1, steps + 1):
         c.step(oracle, t)
     c.compare()

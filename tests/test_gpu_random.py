@@ -1,6 +1,7 @@
-"""Seeded random configurations through the staged and direct kernels against
-the oracle: tensor lists with empty and odd-sized tensors, rank counts from 1
-to 130, one to three gathered outputs, one to three micro-steps."""
+"""Seeded random configurations through the staged and direct fused kernels
+and through the unfused entry points, against the oracle: tensor lists with
+empty and odd-sized tensors, rank counts from 1 to 130, one to three gathered
+outputs, one to three micro-steps."""
 import random
 
 import pytest
@@ -36,14 +37,15 @@ def configs(n, seed):
     return out
 
 
-@pytest.mark.parametrize("kernel", ["staged", "direct"])
+@pytest.mark.parametrize("kernel", ["staged", "direct", "unfused"])
 @pytest.mark.parametrize("idx,numels,n_ranks,n_out,n_micro", configs(12, 20261202))
 def test_random_configuration(oracle, monkeypatch, kernel, idx, numels, n_ranks, n_out, n_micro):
     if kernel == "direct":
         monkeypatch.setenv("ZERO_STEP_KERNEL", "direct")
     else:
         monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
-    c = Case(numels, n_ranks, n_out=n_out, n_micro=n_micro, tag=("random", idx))
+    c = Case(numels, n_ranks, n_out=n_out, n_micro=n_micro, tag=("random", idx),
+             path="unfused" if kernel == "unfused" else "fused")
     for t in (1, 2):
         c.step(oracle, t)
     c.compare()
