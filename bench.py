@@ -45,6 +45,7 @@ WORKLOAD_NAMES = {
     "gpt2-small": "gpt2-small-124M-13units-Nd8",
     "llama3-8b-layer": "llama3-8b-decoder-layer-218M-Nd64",
     "7.5b": "7.5B-32units-Nd64",
+    "7.5b-accum": "7.5B-32units-Nd64-fp32-accum-4-micro",
     "tiny": "tiny-4.2M-Nd4",
 }
 
@@ -118,9 +119,18 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def recorded_traffic(workload: str):
-    """DRAM bytes per launch of the fused kernel from a committed ncu summary,
-    or None when the kernel sources changed since the counters were taken."""
+def traffic_class(n_ranks: int, aligned: bool) -> str:
+    """Kernel form a launch runs, as far as its DRAM traffic per element goes:
+    the rank count and whether every shard starts on the 16-byte grid."""
+    return f"nd{n_ranks}-{'aligned' if aligned else 'misaligned'}"
+
+
+def recorded_traffic(tclass: str, padded_elements: int):
+    """DRAM bytes the fused kernel moves for `padded_elements` flat elements,
+    scaled from a committed ncu capture of a small case of the same kernel form
+    (DRAM read + write bytes per padded element; the kernel streams every
+    element once, so traffic grows in proportion to the elements).  None when
+    no capture of that form exists or the kernel sources changed since."""
     path = os.path.join(ROOT, "profiles", "fused_step_traffic.json")
     try:
         with open(path) as f:
@@ -129,12 +139,16 @@ def recorded_traffic(workload: str):
         return None
     if d.get("kernel_source_hash") != kernel_source_hash():
         return None
-    entry = d.get("workloads", {}).get(workload)
-    return None if entry is None else float(entry["dram_bytes_per_launch"])
+    entry = d.get("captures", {}).get(tclass)
+    if entry is None:
+        return None
+    return float(entry["dram_bytes_per_padded_element"]) * padded_elements
 
 
 class ClockSampler:
-    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks and throttle reasons sampled every 100 ms; each sample
+    is stamped with the host time it arrived, so that a summary can be taken
+    over chosen time windows (the timed regions) only."""
     FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -158,9 +172,11 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.time(), line.strip()))
 
-    def stop(self):
+    def stop(self, windows=None):
+        """Stop sampling; summarise the samples inside `windows` (a list of
+        (t0, t1) host times), or all of them."""
         if self.proc is None:
             return None
         self.proc.terminate()
@@ -169,15 +185,21 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.thread.join(timeout=2)
-        sm, smax, reasons = [], None, set()
+        return self.summary(windows)
+
+    def summary(self, windows=None):
+        sm, power, smax, reasons = [], [], None, set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ln in self.lines:
+        for ts, ln in self.lines:
+            if windows is not None and not any(a <= ts <= b for a, b in windows):
+                continue
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
             try:
                 sm.append(float(parts[0]))
                 smax = float(parts[1])
+                power.append(float(parts[2]))
             except ValueError:
                 continue
             for name, val in zip(names, parts[4:8]):
@@ -186,7 +208,7 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "sm_mhz_min": min(sm), "power_w_max": max(power)}
 
 
 # ------------------------------------------------------------- workloads ----
@@ -459,13 +481,14 @@ def time_resident(res, steps, warmup, ws, device, per_kernel=True, clocks=None):
     return elapsed_max, kern, launches, clock_info
 
 
-def time_graph(step_fn, n_steps, reps=5):
+def time_graph(step_fn, n_steps, reps=5, windows=None):
     """Seconds per step of step_fn(t) replayed from a CUDA graph of n_steps
     consecutive steps: the kernels run back to back, without the host's
     per-call launch cost (tens of microseconds through Python and ctypes),
     which would otherwise hide short kernels.  The graph fixes the step
     number t of every captured call; the bytes and the work do not depend on
-    it.  The step is warmed up eagerly first (kernel attributes, caches)."""
+    it.  The step is warmed up eagerly first (kernel attributes, caches).
+    The host times of the timed replays are appended to `windows`."""
     import torch
     step_fn(1)
     torch.cuda.synchronize()
@@ -476,11 +499,14 @@ def time_graph(step_fn, n_steps, reps=5):
     g.replay()
     torch.cuda.synchronize()
     a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    t0 = time.time()
     a.record()
     for _ in range(reps):
         g.replay()
     b.record()
     torch.cuda.synchronize()
+    if windows is not None:
+        windows.append((t0, time.time()))
     del g
     return a.elapsed_time(b) / 1e3 / (reps * n_steps)
 
@@ -542,6 +568,77 @@ def time_e2e(res, steps, warmup, ws, device):
     barrier(ws)
     el = max_over_ranks(start.elapsed_time(stop) / 1e3, ws, device)
     del host_g, host_p, spare, sets
+    return el, h2d, d2h
+
+
+def time_e2e_streamed(res, steps, warmup, ws, device):
+    """The 7.5B step end to end with gradients streamed unit by unit from host
+    memory, as the model's units would arrive: every step, each of the 32
+    units' N_d gradient rows (N_d x P_pad bf16, 30 GB) crosses the host link
+    into one of two device gradient buffers, the unit is stepped from it
+    (zero_step_units_host, one unit per call), and its gathered bf16 parameters
+    cross back into the unit's pinned host buffer.  Unit i's copy overlaps the
+    step of unit i - 1; a buffer is refilled only after the step that read it.
+    The host holds one set of gradient rows that every unit reads in turn (the
+    resident step also shares one gradient buffer between its units); every
+    byte still crosses the link each time.  Transfers go through the SMs
+    (ZERO_HOST_SM_COPY)."""
+    import torch
+    from fsdp_sharded_mixed_flatten_gb300 import (ZERO_HOST_GRADS_FREE, ZERO_HOST_SM_COPY,
+                                                  HostTables, synthetic, zero_step_units_host)
+    from fsdp_sharded_mixed_flatten_gb300.buffers import aligned_rows, rows
+    from fsdp_sharded_mixed_flatten_gb300.zero import prepare_units
+    hp = dict(synthetic.ADAMW_DEFAULTS)
+    fu0 = res.units[0]
+    N, P_pad = fu0.n_ranks, fu0.P_pad
+    host_g = torch.empty((N, P_pad), dtype=torch.bfloat16, pin_memory=True)
+    for k in range(N):
+        host_g[k].copy_(fu0.grads[k])
+    host_p = [torch.empty(fu.P_pad, dtype=torch.bfloat16, pin_memory=True) for fu in res.units]
+    spare = aligned_rows(N, P_pad, torch.bfloat16, device, 0)
+    dev_sets = (fu0.grad_rows(), rows(spare))
+    prepared = [[prepare_units([(g, *fu.state_rows(), None, fu.param_rows(), fu.layout)])
+                 for g in dev_sets] for fu in res.units]
+    host_rows = [host_g[k] for k in range(N)]
+    tables = [HostTables([host_rows], [hp_buf]) for hp_buf in host_p]
+    h2d = len(res.units) * N * P_pad * 2
+    d2h = sum(fu.P_pad * 2 for fu in res.units)
+    comp = torch.cuda.current_stream()
+    s_h2d, s_d2h = torch.cuda.Stream(), torch.cuda.Stream()
+    done = {}
+    counter = [0]
+
+    def one_step(t):
+        for ui in range(len(res.units)):
+            i = counter[0]
+            counter[0] += 1
+            if i - 2 in done:
+                s_h2d.wait_event(done.pop(i - 2))    # the step that last read this buffer
+            zero_step_units_host(prepared[ui][i % 2], tables[ui], 1, 1, dict(hp, step=t),
+                                 ZERO_HOST_GRADS_FREE | ZERO_HOST_SM_COPY, s_h2d, comp, s_d2h)
+            done[i] = comp.record_event()
+
+    t = 1000
+    for _ in range(warmup):
+        t += 1
+        one_step(t)
+    torch.cuda.synchronize()
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(ws)
+    torch.cuda.nvtx.range_push("timed_e2e")
+    start.record(comp)
+    s_h2d.wait_stream(comp)
+    for _ in range(steps):
+        t += 1
+        one_step(t)
+    comp.wait_stream(s_h2d)
+    comp.wait_stream(s_d2h)
+    stop.record(comp)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    barrier(ws)
+    el = max_over_ranks(start.elapsed_time(stop) / 1e3, ws, device)
+    del host_g, host_p, spare, prepared, tables, dev_sets
     return el, h2d, d2h
 
 
@@ -611,12 +708,16 @@ class OracleRun:
         self.pool.shutdown()
 
 
-def cpu_baseline(seconds=8.0):
+def cpu_baseline(workload="7.5b", seconds=8.0):
     """The CPU oracle as it stands, on a bounded contiguous sample of the
-    gpt2-small workload (all 8 ranks): one chunk of 2^20 flat elements per
-    host core, the chunks stepped in parallel."""
+    workload (all N_d ranks): one chunk per host core of 2^23 / N_d flat
+    elements (so that a chunk holds 2^23 gradient values whatever N_d is), the
+    chunks stepped in parallel for about `seconds`."""
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
     threads = host_threads()
-    run = OracleRun(threads << 20, threads)
+    n_ranks = synthetic.workload(workload).n_ranks
+    per = max(1 << 12, (1 << 23) // n_ranks) & ~7
+    run = OracleRun(threads * per, threads, workload)
     reps, step = 0, 0
     t0 = time.perf_counter()
     while True:
@@ -631,7 +732,7 @@ def cpu_baseline(seconds=8.0):
     return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
             "cpu": cpu_model(),
             "extrapolated_full_step_s": sum(u.numel for u in run.w.units) / rate,
-            "sample": f"{run.E} contiguous flat elements x {run.w.n_ranks} ranks of the gpt2-small "
+            "sample": f"{run.E} contiguous flat elements x {run.w.n_ranks} ranks of the {workload} "
                       f"workload in {len(run.chunks)} chunks, one per thread; {reps} oracle steps "
                       f"in {el:.1f} s (double arithmetic)"}
 
@@ -652,7 +753,8 @@ def run_reference(args, ws, rank, budget_s=90.0):
     rate = 2 * cal.E / (time.perf_counter() - t0)          # elements per second
     cal.close()
     E = int(budget_s * rate / (args.steps + args.warmup))
-    E = max(threads << 10, min(threads << 21, E)) & ~7
+    n_ranks = cal.w.n_ranks
+    E = max(threads << 10, min(threads << 21, (threads << 25) // n_ranks, E)) & ~7
     run = OracleRun(E, threads, args.workload)
     step = 0
     for _ in range(args.warmup):
@@ -770,6 +872,74 @@ def run_sweep(args, device, hbm_peak):
     return 0
 
 
+L2_BYTES = 129e6
+
+
+def sweep_points(gated_only=False):
+    """(P, N_d, fused bytes per step, gated) of the flat-size x N_d sweep; a
+    point is gated when its step moves at least 4 x L2 (smaller ones stay
+    partly cache-resident between steps)."""
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    out = []
+    for P in synthetic.sweep_sizes():
+        for n in synthetic.SWEEP_RANKS:
+            nbytes = unit_bytes(synthetic.padded(P, n), n)
+            gated = nbytes >= 4 * L2_BYTES
+            if gated or not gated_only:
+                out.append((P, n, nbytes, gated))
+    return out
+
+
+def sweep_gated(device, hbm_peak, local, min_seconds=0.25):
+    """The sweep's gated points, timed in the default run: for each (P, N_d)
+    the fused step (one zero_step launch of the staged kernel) replayed from a
+    CUDA graph (the kernels back to back; at least 10 steps and min_seconds of
+    timed replays) and, beside it, timed eagerly with per-launch CUDA events
+    (one Python call per step, at least 10 steps).  Clocks are sampled over
+    the whole sweep and summarised over the timed windows only."""
+    import gc
+    import torch
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
+    hp0 = dict(synthetic.ADAMW_DEFAULTS)
+    sampler = ClockSampler(local).start()
+    windows, points = [], []
+    for P, n, nbytes, _ in sweep_points(gated_only=True):
+        res = Resident(synthetic.workload(f"sweep:{P}:{n}"))
+        fu = res.units[0]
+        # a rough step time from a few eager steps sizes both timings
+        el, kern, _, _ = time_resident(res, 3, 3, 1, device)
+        est = max(kern / 3, 1e-6)
+        eager_steps = int(max(10, min(2000, min_seconds / est)))
+        t0 = time.time()
+        el, kern, _, _ = time_resident(res, eager_steps, 2, 1, device)
+        windows.append((t0, time.time()))
+        n_graph = int(max(4, min(50, 5e9 // nbytes)))
+        reps = int(max(3, -(-10 // n_graph), min_seconds / (est * n_graph)))
+        g = time_graph(lambda t: res.launch(t, hp0), n_graph, reps, windows)
+        points.append({"P": P, "n_ranks": n, "S_mod_8": fu.S % 8, "bytes_per_step": nbytes,
+                       "graph_steps": n_graph * reps, "graph_ms": g * 1e3,
+                       "graph_frac_of_measured_hbm": nbytes / g / 1e9 / hbm_peak,
+                       "eager_steps": eager_steps, "eager_kernel_ms": kern / eager_steps * 1e3,
+                       "eager_frac_of_measured_hbm": nbytes * eager_steps / kern / 1e9 / hbm_peak})
+        del res, fu
+        gc.collect()
+    clock_info = sampler.stop(windows)
+    torch.cuda.empty_cache()
+    worst = min(points, key=lambda p: p["graph_frac_of_measured_hbm"])
+    return {"gate": "fused step >= 0.80 of the measured HBM copy peak on every point moving "
+                    ">= 4 x L2 per step",
+            "timing": "graph: CUDA-graph replays of the fused launch, kernels back to back "
+                      "(the gated figure); eager: per-launch CUDA events, one Python call per step",
+            "n_points": len(points),
+            "min_graph_frac_of_measured_hbm": worst["graph_frac_of_measured_hbm"],
+            "min_point": f"P={worst['P']} N_d={worst['n_ranks']}",
+            "min_eager_frac_of_measured_hbm": min(p["eager_frac_of_measured_hbm"]
+                                                  for p in points),
+            "points_at_or_above_0.80": sum(p["graph_frac_of_measured_hbm"] >= 0.80
+                                           for p in points),
+            "clocks": clock_info, "points": points}
+
+
 def zero1_vs_zero2(device, hbm_peak, n_micro=4, steps=2):
     """One optimizer step of K = 4 micro-batches on the Llama-3-8B layer
     (N_d = 64) in the ZeRO-2 form (reduce-scatter into the sharded fp32
@@ -824,6 +994,7 @@ def zero1_vs_zero2(device, hbm_peak, n_micro=4, steps=2):
 
 
 def run_ours(args, ws, rank, local):
+    import gc
     import torch
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device for --impl ours")
@@ -838,6 +1009,7 @@ def run_ours(args, ws, rank, local):
         return run_sweep(args, device, hbm_peak)
 
     w = synthetic.workload(args.workload)
+    streamed = args.workload.startswith("7.5b")      # one gradient buffer for every unit
     if args.variant == "clip":
         res = ClipResident(w, max_norm=1.0)
     elif args.variant == "per-param":
@@ -845,46 +1017,69 @@ def run_ours(args, ws, rank, local):
     elif args.variant == "zero1":
         res = Zero1Resident(w)
     else:
-        res = Resident(w)
+        res = Resident(w, shared_grads=streamed)
     clocks = ClockSampler(local)
     el, kern, launches, clock_info = time_resident(res, args.steps, args.warmup, ws, device,
                                                    clocks=clocks)
     value = ws * res.numel * args.steps / el
+    n_launch = res.launches_per_step
     achieved = res.bytes * args.steps / kern / 1e9
-    traffic = recorded_traffic(args.workload) if args.variant == "plain" else None
-    n_launch = len(res.units)
+    traffic = None
+    if args.variant == "plain" and w.n_micro == 1:
+        aligned = all(fu.S % 8 == 0 for fu in res.units)
+        traffic = recorded_traffic(traffic_class(w.n_ranks, aligned),
+                                   sum(fu.P_pad for fu in res.units))
     e2e = None
-    if not args.no_e2e and args.variant == "plain":
-        e2e_el, h2d, d2h = time_e2e(res, args.steps, args.warmup, ws, device)
-        e2e = {"value": ws * res.numel * args.steps / e2e_el, "unit": UNIT,
+    if not args.no_e2e and args.variant == "plain" and w.n_micro == 1:
+        if streamed:
+            e2e_steps, e2e_warm = min(args.steps, 3), 1
+            e2e_el, h2d, d2h = time_e2e_streamed(res, e2e_steps, e2e_warm, ws, device)
+            how = ("every unit's gradient rows copied in and its parameters copied out each step, "
+                   "unit by unit through two device gradient buffers; SM loads/stores through "
+                   "the pinned buffers' device mapping (ZERO_HOST_SM_COPY)")
+        else:
+            e2e_steps, e2e_warm = args.steps, args.warmup
+            e2e_el, h2d, d2h = time_e2e(res, e2e_steps, e2e_warm, ws, device)
+            how = ("SM loads/stores through the pinned buffers' device mapping "
+                   "(ZERO_HOST_SM_COPY)")
+        e2e = {"value": ws * res.numel * e2e_steps / e2e_el, "unit": UNIT,
                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-               "transport": "SM loads/stores through the pinned buffers' device mapping "
-                            "(ZERO_HOST_SM_COPY)"}
+               "steps": e2e_steps, "warmup": e2e_warm, "ms_per_step": e2e_el / e2e_steps * 1e3,
+               "transport": how}
     step_bytes = res.bytes
+    units_desc = {"units": len(res.units), "params": res.numel,
+                  "padded_elements": sum(getattr(fu, "P_pad", getattr(fu, "numel", 0))
+                                         for fu in res.units)}
+    grad_bytes = w.n_ranks * sum(synthetic.padded(u.numel, w.n_ranks) for u in
+                                 (w.units[:1] if streamed else w.units)) * 2
     del res
-    import gc
     gc.collect()
     torch.cuda.empty_cache()
 
     extra = {}
     if not args.no_extra:
-        extra["llama3-8b-decoder-layer-Nd64"] = secondary("llama3-8b-layer", 5, 3, ws, device,
+        if args.workload != "7.5b":
+            extra["7.5B-32units-Nd64-streamed-grads"] = secondary("7.5b", 5, 3, ws, device,
+                                                                  hbm_peak, shared=True)
+        if args.workload != "gpt2-small":
+            extra["gpt2-small-124M-13units-Nd8"] = secondary("gpt2-small", 20, 3, ws, device,
+                                                             hbm_peak)
+        extra["llama3-8b-decoder-layer-Nd64"] = secondary("llama3-8b-layer", 10, 3, ws, device,
                                                           hbm_peak)
-        extra["7.5B-32units-Nd64-streamed-grads"] = secondary("7.5b", 2, 1, ws, device,
-                                                              hbm_peak, shared=True)
         extra["7.5B-32units-Nd64-fp32-accum-4-micro"] = secondary("7.5b-accum", 2, 1, ws, device,
                                                                   hbm_peak, shared=True)
-
         extra["llama3-8b-layer-K4-zero2-vs-zero1"] = zero1_vs_zero2(device, hbm_peak)
-        from fsdp_sharded_mixed_flatten_gb300 import synthetic as _syn
         extra["gpt2-small-global-norm-clip"] = timed_extra(
-            ClipResident(_syn.workload("gpt2-small"), max_norm=1.0), 20, 3, ws, device, hbm_peak)
+            ClipResident(synthetic.workload("gpt2-small"), max_norm=1.0), 20, 3, ws, device,
+            hbm_peak)
         extra["gpt2-small-fsdp2-per-parameter-148-units"] = timed_extra(
-            PerParamResident(_syn.workload("gpt2-small")), 20, 3, ws, device, hbm_peak)
+            PerParamResident(synthetic.workload("gpt2-small")), 20, 3, ws, device, hbm_peak)
         extra["llama3-8b-layer-fsdp2-per-parameter-9-units"] = timed_extra(
-            PerParamResident(_syn.workload("llama3-8b-layer")), 5, 3, ws, device, hbm_peak)
+            PerParamResident(synthetic.workload("llama3-8b-layer")), 5, 3, ws, device, hbm_peak)
+        if not args.no_sweep:
+            extra["sweep_gated"] = sweep_gated(device, hbm_peak, local)
 
-    base = cpu_baseline() if (rank == 0 and ws == 1 and not args.no_cpu) else None
+    base = cpu_baseline(args.workload) if (rank == 0 and ws == 1 and not args.no_cpu) else None
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
@@ -892,20 +1087,26 @@ def run_ours(args, ws, rank, local):
         "data": "synthetic",
         "config": {"workload": workload_label(args.workload), "variant": args.variant,
                    "seed": args.seed,
-                   "n_ranks_logical": w.n_ranks,
-                   "units": n_launch, "params": sum(u.numel for u in w.units),
+                   "n_ranks_logical": w.n_ranks, **units_desc,
                    "storage": "bf16 grads/params, fp32 master/m/v", "n_out": 1,
                    "bytes_per_step": step_bytes,
                    "hbm_gbs_per_step": step_bytes / (el / args.steps) / 1e9,
-                   "l2": "inputs larger than L2 (%.2f GB of gradients per step)" % (
-                       w.n_ranks * sum(synthetic.padded(u.numel, w.n_ranks) for u in w.units)
-                       * 2 / 1e9),
+                   "l2": "inputs larger than L2 (%.2f GB of gradients read per unit pass)" % (
+                       grad_bytes / 1e9),
+                   "gradients": ("one N_d x P_pad buffer read by every unit in turn (streamed "
+                                 "unit by unit)" if streamed else "resident per unit"),
                    "parallelism": f"replicas x{ws}" if ws > 1 else "1 GPU, N_d logical ranks"},
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": hbm_peak, "unit": "GB/s",
                      "frac": achieved / hbm_peak, "peak_kind": peak_kind,
                      "kernel": ("fused_step_kernel" if os.environ.get("ZERO_STEP_KERNEL") == "direct"
                                 else "staged_step_kernel"),
-                     "traffic": traffic * 1.0 if traffic is not None else None},
+                     "launches_per_step": n_launch,
+                     "algorithmic_bytes_per_launch": step_bytes / n_launch,
+                     "traffic": traffic / n_launch if traffic is not None else None,
+                     "traffic_source": ("DRAM read+write bytes per padded element from a small "
+                                        "ncu capture of the same kernel form, scaled to this "
+                                        "launch's elements (profiles/fused_step_traffic.json)")
+                     if traffic is not None else None},
         "cpu_baseline": base,
         "e2e": e2e,
         "gpu_launches": launches,
@@ -923,17 +1124,20 @@ def run_ours(args, ws, rank, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="gpt2-small",
-                    help="gpt2-small | llama3-8b-layer | 7.5b | tiny | sweep:<P>:<N_d>")
+    ap.add_argument("--workload", default="7.5b",
+                    help="7.5b (default) | 7.5b-accum | gpt2-small | llama3-8b-layer | tiny | "
+                         "sweep:<P>:<N_d>")
     ap.add_argument("--variant", default="plain", choices=["plain", "clip", "per-param", "zero1"],
                     help="the timed step: plain (default), with global-norm clipping, as FSDP2 "
                          "per-parameter units, or the ZeRO-1 form of 4 micro-steps (first unit)")
     ap.add_argument("--no-extra", action="store_true", help="skip the secondary workloads")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer leg")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the gated sweep points of the default run")
     ap.add_argument("--sweep", action="store_true",
                     help="fused vs unfused over the flat-size x N_d sweep (JSON line per point)")
     ap.add_argument("--sweep-sizes", default="", help="comma-separated flat sizes for --sweep")
