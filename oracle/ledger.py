@@ -4,117 +4,122 @@ TEST INFRASTRUCTURE ONLY (see ``oracle/__init__.py``).
 
 Sources (page title, section):
   [L5] "Lesson 5: ZeRO and FSDP (including the FSDP2 architecture)",
-       hpc.payai.win -- section 2 (per-rank memory M0..M3 with the optimizer
-       multiplier k = 12 and the fp32 gradient-accumulation note), section 3
-       (communication: V_RS = V_AG = (N_d-1)/N_d * Psi; DDP 2 Psi; ZeRO-1/2
-       2 Psi; ZeRO-3 3 Psi), the worked 7B table that follows section 7.
+       hpc.payai.win -- section 2 (per-rank memory of stages 0..3 with the
+       optimizer's 12 bytes per parameter, and the note on an fp32 gradient
+       accumulator), section 3 (communication: one reduce-scatter or one
+       all-gather moves (N_d-1)/N_d * Psi per rank; DDP and ZeRO-1/2 move
+       2 Psi, ZeRO-3 3 Psi), the worked 7B table that follows section 7.
   [DZ] "Data parallelism and ZeRO memory sharding", jefxiong.cn -- section 3.2
-       (16 bytes per parameter: 2 + 2 + 4 + 4 + 4), section 3.3 (the three
-       stage formulas and the 7.5B / 64-rank example), section 3.4
-       (reduce-scatter + all-gather make the all-reduce), section 4.1 (printed
-       ledgers for 7.5B/64 and 1.5B/8, decimal GB).
+       (16 bytes per parameter: 2 + 2 + 4 + 4 + 4), section 3.3 (the stage
+       formulas and the 7.5B / 64-rank example), section 3.4 (reduce-scatter
+       + all-gather make the all-reduce), section 4.1 (printed ledgers for
+       7.5B/64 and 1.5B/8, decimal GB).
   [ZvF] "ZeRO vs FSDP: memory accounting and communication breakdown for
        large-model distributed training", muhenan.com -- sections 1 and 2
        (16N GB for N billion parameters; 70B on 64 GPUs ~ 17.5 GB).
 
-Sizes are in bytes; GB means 1e9 bytes, as on the pages.
+The memory side is one table: every kind of model state with its bytes per
+parameter and the lowest ZeRO stage that partitions it over the ranks.  A
+rank holds each kind whole below that stage and a 1/N_d share from it on;
+stage 0 is plain data parallelism.  Sizes are in bytes; GB means 1e9 bytes,
+as on the pages.
 """
 from __future__ import annotations
 
-# Bytes per parameter of each model-state kind under bf16/fp16 mixed-precision
-# Adam ([DZ] section 3.2).
-PARAM_BYTES = 2          # low-precision parameters
-GRAD_BYTES = 2           # low-precision gradients
-MASTER_BYTES = 4         # fp32 master weights
-MOMENT_BYTES = 4         # each of Adam's m and v
-OPTIMIZER_MULTIPLIER = MASTER_BYTES + 2 * MOMENT_BYTES   # k = 12 ([L5] section 2)
-FP32_ACCUM_BYTES = 4     # fp32 gradient accumulator ([L5] section 2, note)
+from collections import namedtuple
 
-STAGES = (0, 1, 2, 3)    # 0 = plain data parallel (DDP)
+StateKind = namedtuple("StateKind", "name bytes_per_param sharded_from_stage")
+
+# Mixed-precision Adam ([DZ] section 3.2; [L5] section 2): the low-precision
+# parameters are partitioned by stage 3, the low-precision gradients by
+# stage 2, and the fp32 optimizer state (master weights, m, v: 4 + 4 + 4) by
+# stage 1.
+MODEL_STATE = (
+    StateKind("parameters", 2, 3),
+    StateKind("gradients", 2, 2),
+    StateKind("optimizer", 12, 1),
+)
+# An fp32 gradient accumulator for micro-batching follows the gradients: whole
+# while they are whole (stages 0 and 1), partitioned with them from stage 2
+# ([L5] section 2, note).
+FP32_ACCUMULATOR = StateKind("fp32 accumulator", 4, 2)
+
+KIND_BYTES = {k.name: k.bytes_per_param for k in MODEL_STATE + (FP32_ACCUMULATOR,)}
+STAGES = (0, 1, 2, 3)
 
 
-def _check(psi, n):
-    if psi <= 0 or n <= 0:
-        raise ValueError("parameter count and rank count must be positive")
+def _require(psi, n):
+    if not (psi > 0 and n > 0):
+        raise ValueError(f"ledger needs psi > 0 and n > 0 (got psi={psi!r}, n={n!r})")
 
 
-def model_state_bytes(psi: float, n: int, stage: int, k: float = OPTIMIZER_MULTIPLIER,
-                      fp32_grad_accum: bool = False) -> float:
-    """Per-rank model-state bytes for ZeRO stage 0..3 ([L5] section 2).
-
-    stage 0: 2Psi + 2Psi + k Psi                 (everything replicated)
-    stage 1: 2Psi + 2Psi + k Psi / n             (optimizer state sharded)
-    stage 2: 2Psi + (2Psi + k Psi) / n           (+ gradients sharded)
-    stage 3: (2Psi + 2Psi + k Psi) / n           (+ parameters sharded)
-    The optional fp32 accumulator is replicated for stages 0 and 1 (+4 Psi)
-    and sharded for stages 2 and 3 (+4 Psi / n).
-    """
-    _check(psi, n)
+def _require_stage(stage):
     if stage not in STAGES:
-        raise ValueError("stage must be 0..3")
-    params = PARAM_BYTES * psi
-    grads = GRAD_BYTES * psi
-    optim = k * psi
-    if stage == 0:
-        total = params + grads + optim
-    elif stage == 1:
-        total = params + grads + optim / n
-    elif stage == 2:
-        total = params + (grads + optim) / n
-    else:
-        total = (params + grads + optim) / n
-    if fp32_grad_accum:
-        total += FP32_ACCUM_BYTES * psi if stage <= 1 else FP32_ACCUM_BYTES * psi / n
-    return total
+        raise ValueError(f"no ZeRO stage {stage!r}: use 0 (replicated) to 3")
+
+
+def held_fraction(kind: StateKind, n: int, stage: int) -> float:
+    """The share of one state kind a rank keeps: all of it below the stage that
+    partitions it, 1/n from that stage on."""
+    return 1.0 / n if stage >= kind.sharded_from_stage else 1.0
+
+
+def per_rank_state_bytes(psi: float, n: int, stage: int, accumulator: bool = False) -> float:
+    """Model-state bytes one of n ranks holds for psi parameters under a ZeRO
+    stage ([L5] section 2; [DZ] section 3.3): the sum over the state table of
+    bytes per parameter x psi x the share the rank keeps."""
+    _require(psi, n)
+    _require_stage(stage)
+    kinds = MODEL_STATE + ((FP32_ACCUMULATOR,) if accumulator else ())
+    return sum(k.bytes_per_param * psi * held_fraction(k, n, stage) for k in kinds)
 
 
 def bytes_per_param(n: int, stage: int) -> float:
     """Per-rank model-state bytes divided by the parameter count."""
-    return model_state_bytes(1.0, n, stage)
+    return per_rank_state_bytes(1.0, n, stage)
 
 
 def memory_saving(n: int, stage: int) -> float:
     """How many times smaller the per-rank state is than plain data parallel."""
-    return model_state_bytes(1.0, n, 0) / model_state_bytes(1.0, n, stage)
+    return per_rank_state_bytes(1.0, n, 0) / per_rank_state_bytes(1.0, n, stage)
 
 
 def collective_volume(psi: float, n: int) -> float:
     """Elements each rank moves in one reduce-scatter or one all-gather of Psi
     elements over n ranks (ring model, [L5] section 3; [DZ] section 3.4)."""
-    _check(psi, n)
+    _require(psi, n)
     return (n - 1) / n * psi
 
 
-def comm_elements(psi: float, n: int, stage: int, exact: bool = True) -> float:
-    """Elements moved per rank per training step ([L5] section 3).
+# Collectives of one training step per stage ([L5] section 3): an all-reduce
+# is a reduce-scatter plus an all-gather; ZeRO-1/2 reduce-scatter the
+# gradients and all-gather the updated parameters; ZeRO-3 also all-gathers the
+# parameters a second time for the backward pass.
+COLLECTIVES_PER_STEP = {0: 2, 1: 2, 2: 2, 3: 3}
 
-    stage 0: all-reduce = reduce-scatter + all-gather
-    stage 1/2: reduce-scatter of gradients + all-gather of updated parameters
-    stage 3: forward all-gather + backward all-gather + reduce-scatter
-    exact=False gives the pages' large-n approximations 2 Psi and 3 Psi.
-    """
-    _check(psi, n)
-    if stage not in STAGES:
-        raise ValueError("stage must be 0..3")
-    one = collective_volume(psi, n) if exact else psi
-    if stage in (0, 1, 2):
-        return 2 * one
-    return 3 * one
+
+def comm_elements(psi: float, n: int, stage: int, exact: bool = True) -> float:
+    """Elements moved per rank per training step.  exact=False takes each
+    collective as a full Psi, the pages' large-n forms 2 Psi and 3 Psi."""
+    _require(psi, n)
+    _require_stage(stage)
+    per_collective = collective_volume(psi, n) if exact else psi
+    return COLLECTIVES_PER_STEP[stage] * per_collective
 
 
 def comm_bytes(psi: float, n: int, stage: int, exact: bool = False,
-               bytes_per_element: int = GRAD_BYTES) -> float:
+               bytes_per_element: int = KIND_BYTES["gradients"]) -> float:
     """Bytes per rank per step; the pages count 2-byte (bf16/fp16) elements."""
     return comm_elements(psi, n, stage, exact=exact) * bytes_per_element
 
 
 def adam_scalars_per_rank(psi: int, n: int, sharded: bool) -> int:
     """Number of Adam m and v scalars a rank holds ([DZ] section 4.2)."""
-    if sharded:
-        if psi % n:
-            raise ValueError("the shard count must divide the parameter count")
-        return 2 * (psi // n)
-    return 2 * psi
+    if not sharded:
+        return 2 * psi
+    if psi % n:
+        raise ValueError(f"{n} shards do not divide {psi} parameters evenly")
+    return 2 * (psi // n)
 
 
 def gb(nbytes: float) -> float:
@@ -122,11 +127,16 @@ def gb(nbytes: float) -> float:
     return nbytes / 1e9
 
 
+StageLedger = namedtuple("StageLedger", "stage state_gb bytes_per_param saving_vs_ddp comm_gb")
+
+
 def ledger_rows(psi: float, n: int):
-    """Rows (stage, bytes/param, state GB, saving vs DDP, comm GB per step) in
-    the layout of the printed ledgers of [DZ] section 4.1 (approximate comm)."""
-    rows = []
-    for stage in STAGES:
-        rows.append((stage, bytes_per_param(n, stage), gb(model_state_bytes(psi, n, stage)),
-                     memory_saving(n, stage), gb(comm_bytes(psi, n, stage, exact=False))))
-    return rows
+    """One StageLedger per stage 0..3 for psi parameters on n ranks: the
+    per-rank model state in GB and per parameter, the saving against plain
+    data parallel, and the approximate communication per step in GB (the
+    quantities [DZ] section 4.1 prints)."""
+    return [StageLedger(stage=s, state_gb=gb(per_rank_state_bytes(psi, n, s)),
+                        bytes_per_param=bytes_per_param(n, s),
+                        saving_vs_ddp=memory_saving(n, s),
+                        comm_gb=gb(comm_bytes(psi, n, s, exact=False)))
+            for s in STAGES]

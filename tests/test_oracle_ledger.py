@@ -23,14 +23,14 @@ def test_printed_ledgers(name):
     psi, n, table, exact = _ledger_fixture(name)
     rows = ledger.ledger_rows(psi, n)
     assert len(rows) == len(table) == 4
-    for (stage, bpp, state_gb, saving, comm_gb), ref in zip(rows, table):
-        assert int(ref[0]) == stage
-        assert f"{bpp:.4f}" == ref[1]
-        assert f"{state_gb:.2f}" == ref[2]
-        assert f"{saving:.2f}" == ref[3]
-        assert f"{comm_gb:.2f}" == ref[4]
+    for row, ref in zip(rows, table):
+        assert int(ref[0]) == row.stage
+        assert f"{row.bytes_per_param:.4f}" == ref[1]
+        assert f"{row.state_gb:.2f}" == ref[2]
+        assert f"{row.saving_vs_ddp:.2f}" == ref[3]
+        assert f"{row.comm_gb:.2f}" == ref[4]
     for _, stage, value in exact:
-        got = ledger.gb(ledger.model_state_bytes(psi, n, int(stage)))
+        got = ledger.gb(ledger.per_rank_state_bytes(psi, n, int(stage)))
         assert got == pytest.approx(float(value), rel=1e-12)
 
 
@@ -41,21 +41,21 @@ def test_7b_worked_table():
         kind = r[0]
         if kind == "printout":
             dp = int(r[1])
-            z = [ledger.gb(ledger.model_state_bytes(psi, dp, s)) for s in (1, 2, 3)]
+            z = [ledger.gb(ledger.per_rank_state_bytes(psi, dp, s)) for s in (1, 2, 3)]
             comm = ledger.comm_elements(psi, dp, 3, exact=False) / 1e9
             assert [f"{x:.1f}" for x in z] + [f"{comm:.1f}"] == r[2:]
         elif kind == "exact":
             dp, stage, val = int(r[1]), int(r[2]), float(r[3])
-            assert ledger.gb(ledger.model_state_bytes(psi, dp, stage)) == pytest.approx(val,
+            assert ledger.gb(ledger.per_rank_state_bytes(psi, dp, stage)) == pytest.approx(val,
                                                                                       rel=1e-12)
         elif kind == "table":
             dp, stage, val = int(r[1]), int(r[2]), float(r[3])
-            got = ledger.gb(ledger.model_state_bytes(psi, dp, stage))
+            got = ledger.gb(ledger.per_rank_state_bytes(psi, dp, stage))
             # the table rounds by hand (26.25 -> 26.3): half-up to one decimal
             assert abs(got - val) <= 0.05 + 1e-9
         elif kind == "psi70":
             dp, stage, val = int(r[1]), int(r[2]), float(r[3])
-            assert ledger.gb(ledger.model_state_bytes(70e9, dp, stage)) == pytest.approx(val)
+            assert ledger.gb(ledger.per_rank_state_bytes(70e9, dp, stage)) == pytest.approx(val)
         elif kind == "comm":
             mult, values, gbytes = int(r[1]), float(r[2]), float(r[3])
             stage = 1 if mult == 2 else 3
@@ -70,7 +70,7 @@ def test_misc_printed_values():
         kind = r[0]
         if kind == "state_gb":
             psi, n, stage, val = float(r[1]), int(r[2]), int(r[3]), float(r[4])
-            assert ledger.gb(ledger.model_state_bytes(psi, n, stage)) == pytest.approx(val)
+            assert ledger.gb(ledger.per_rank_state_bytes(psi, n, stage)) == pytest.approx(val)
         elif kind == "psi_multiple":
             n, stage, mult, pct = int(r[1]), int(r[2]), float(r[3]), int(r[4])
             per = ledger.bytes_per_param(n, stage)
@@ -78,18 +78,18 @@ def test_misc_printed_values():
             assert round(100 * (1 - per / 16)) == pct
         elif kind == "optimizer_share":
             n, val = int(r[1]), float(r[2])
-            assert ledger.OPTIMIZER_MULTIPLIER / n == val
+            assert ledger.KIND_BYTES["optimizer"] / n == val
         elif kind == "parts":
             psi, n, stage = float(r[1]), int(r[2]), int(r[3])
             p_gb, g_gb, o_gb, total = (float(x) for x in r[4:8])
             sharded_p = stage >= 3
             sharded_g = stage >= 2
             sharded_o = stage >= 1
-            got_p = ledger.gb(ledger.PARAM_BYTES * psi / (n if sharded_p else 1))
-            got_g = ledger.gb(ledger.GRAD_BYTES * psi / (n if sharded_g else 1))
-            got_o = ledger.gb(ledger.OPTIMIZER_MULTIPLIER * psi / (n if sharded_o else 1))
+            got_p = ledger.gb(ledger.KIND_BYTES["parameters"] * psi / (n if sharded_p else 1))
+            got_g = ledger.gb(ledger.KIND_BYTES["gradients"] * psi / (n if sharded_g else 1))
+            got_o = ledger.gb(ledger.KIND_BYTES["optimizer"] * psi / (n if sharded_o else 1))
             assert (got_p, got_g, got_o) == pytest.approx((p_gb, g_gb, o_gb))
-            assert ledger.gb(ledger.model_state_bytes(psi, n, stage)) == pytest.approx(total)
+            assert ledger.gb(ledger.per_rank_state_bytes(psi, n, stage)) == pytest.approx(total)
         else:
             raise AssertionError(kind)
 
@@ -97,7 +97,7 @@ def test_misc_printed_values():
 def test_one_rank_all_stages_equal():
     # [L5] answer key: at dp = 1 the three stages hold the same bytes.
     psi = 1_000_000
-    vals = {ledger.model_state_bytes(psi, 1, s) for s in (0, 1, 2, 3)}
+    vals = {ledger.per_rank_state_bytes(psi, 1, s) for s in (0, 1, 2, 3)}
     assert vals == {16 * psi}
 
 
@@ -117,8 +117,8 @@ def test_fp32_accumulation_term():
     # [L5] section 2 note: +4 Psi for stage 1 (gradients unsharded), +4 Psi / N for 2 and 3.
     psi, n = 7e9, 8
     for stage, extra in ((0, 4 * psi), (1, 4 * psi), (2, 4 * psi / n), (3, 4 * psi / n)):
-        d = (ledger.model_state_bytes(psi, n, stage, fp32_grad_accum=True)
-             - ledger.model_state_bytes(psi, n, stage))
+        d = (ledger.per_rank_state_bytes(psi, n, stage, accumulator=True)
+             - ledger.per_rank_state_bytes(psi, n, stage))
         assert d == pytest.approx(extra)
 
 
@@ -148,8 +148,8 @@ def test_adam_scalar_count():
 
 def test_rejects_non_positive():
     with pytest.raises(ValueError):
-        ledger.model_state_bytes(0, 8, 1)
+        ledger.per_rank_state_bytes(0, 8, 1)
     with pytest.raises(ValueError):
-        ledger.model_state_bytes(10, 0, 1)
+        ledger.per_rank_state_bytes(10, 0, 1)
     with pytest.raises(ValueError):
-        ledger.model_state_bytes(10, 8, 4)
+        ledger.per_rank_state_bytes(10, 8, 4)
