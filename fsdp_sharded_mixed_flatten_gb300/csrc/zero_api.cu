@@ -24,7 +24,8 @@
 static_assert(zf::kMaxRanks == ZERO_MAX_RANKS, "rank limit mismatch");
 static_assert(zf::kMaxUnits == ZERO_UNITS_PER_LAUNCH && zf::kMaxPtrs == ZERO_POINTERS_PER_LAUNCH,
               "launch packing limits mismatch");
-static_assert(zf::kDeviceOk == ZERO_DEVICE_OK && zf::kDeviceTimeout == ZERO_DEVICE_TIMEOUT,
+static_assert(zf::kDeviceOk == ZERO_DEVICE_OK && zf::kDeviceTimeout == ZERO_DEVICE_TIMEOUT &&
+                  zf::kDeviceSchedConflict == ZERO_DEVICE_SCHED_CONFLICT,
               "device status codes mismatch");
 // One unit always fits a launch: at most 5 pointers per rank (gradients,
 // master, m, v, accumulator) plus one per gathered output.
@@ -242,6 +243,7 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
     a.h.n_units = 0;
     a.h.total_tiles = 0;
     a.h.grid = 0;
+    a.h.sched_slot = -1;
     a.h.k = k;
     auto flush = [&]() -> int {
         if (a.h.n_units == 0) return ZERO_OK;

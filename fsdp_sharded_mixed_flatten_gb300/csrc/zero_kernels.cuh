@@ -96,6 +96,7 @@ struct MultiHeader {
     int32_t n_units;
     int32_t total_tiles;
     int32_t grid;           // CTAs to launch; 0: the persistent grid for the kernel form
+    int32_t sched_slot;     // dynamic tile scheduling slot (sched_slot), -1: fixed order
     AdamConsts k;
     // global gradient-norm clipping
     double* partials;       // per-CTA sums of squares of the averaged gradient
@@ -135,6 +136,7 @@ enum StepMode : int {
 // Device-side status codes (g_zf_device_status); must match ZERO_DEVICE_*.
 constexpr int kDeviceOk = 0;
 constexpr int kDeviceTimeout = 1;
+constexpr int kDeviceSchedConflict = 2;
 
 // Launchers (return the launch status; grid sizes are chosen inside).
 template <int MAXR>
@@ -148,10 +150,11 @@ cudaError_t launch_all_gather(const ShardArgs<MAXR>& a, cudaStream_t stream);
 cudaError_t launch_flatten(const FlatArgs& a, int elem_bytes, int unflatten, cudaStream_t stream);
 // Bulk-copy staged fused step / reduce-scatter over the units of `a` (mode:
 // StepMode); `n_ptrs` pointers of a.ptrs are in use (picks the block size).
-cudaError_t launch_staged_step(const MultiArgs& a, int n_ptrs, int mode, cudaStream_t stream);
+// Sets a.h.sched_slot (the tile order) for the launch.
+cudaError_t launch_staged_step(MultiArgs& a, int n_ptrs, int mode, cudaStream_t stream);
 // The same, reading fp32 gradient buffers (ZeRO-1 full accumulators; mode
 // kModeMeanDiv only).
-cudaError_t launch_staged_step_f32(const MultiArgs& a, int n_ptrs, cudaStream_t stream);
+cudaError_t launch_staged_step_f32(MultiArgs& a, int n_ptrs, cudaStream_t stream);
 // ZeRO-1 local accumulation of each rank's bf16 gradient into its full fp32
 // accumulator (a.grads -> a.accum, P_pad elements each).
 template <int MAXR>
@@ -164,6 +167,9 @@ cudaError_t launch_zero1_accumulate_staged(const StepArgs<MAXR>& a, int first, c
 // CTA per SM).  A norm launch is given this many CTAs explicitly (h.grid) and
 // writes exactly this many partial sums.
 int staged_grid(int mode, int total_tiles);
+// Dynamic tile-scheduling slot for a staged launch on `stream` (-1: the fixed
+// tile order).
+int sched_slot(cudaStream_t stream);
 // One CTA waiting on a barrier that nothing completes (tests the bounded wait).
 cudaError_t launch_wait_timeout_selftest(uint64_t limit_ns, cudaStream_t stream);
 // Read (and optionally clear) the device status word; synchronises `stream`.

@@ -33,6 +33,9 @@
 // of the CTA to stop, and the CTA waits (bounded again) for the copies it
 // issued before it returns.
 #include <atomic>
+#include <cstdlib>
+#include <mutex>
+#include <vector>
 #include <type_traits>
 
 #include "zero_kernels.cuh"
@@ -40,6 +43,25 @@
 namespace zf {
 
 __device__ int g_zf_device_status = 0;
+
+// Dynamic tile scheduling.  The persistent CTAs of a launch claim tiles from
+// one counter instead of striding through them in a fixed order: measured on
+// GB300, the SMs of a launch whose tiles take one stage each (N_d <= 2, the
+// clipped step's update pass) run at speeds up to 40 % apart, and with a fixed
+// order the fast ones sat idle for the last 15 % of the launch.  Every
+// element's result is the same whichever CTA computes it.  A slot is
+// {next tile, CTAs finished}; the last CTA of a launch to finish puts it back
+// to zero, so the slot is ready for the next launch on the same stream (the
+// host gives every stream a slot of its own; see sched_slot).
+// Slots [0, kStreamSlots): one per (device, stream) for launches made
+// directly; [kStreamSlots, kSharedSlot): launches captured into CUDA graphs,
+// one each in turn; kSharedSlot: every launch while ZERO_SCHED_SHARED is set
+// (failure injection).
+constexpr int kStreamSlots = 1024;
+constexpr int kSchedSlots = 2048;
+constexpr int kSharedSlot = kSchedSlots - 1;
+constexpr int kDynamicMinRounds = 16;
+__device__ unsigned int g_zf_sched[kSchedSlots][2];
 
 namespace {
 
@@ -176,7 +198,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
         if (*abort_flag) return false;
         if (global_timer_ns() - t0 > limit_ns) {
             *abort_flag = 1;
-            atomicExch(&g_zf_device_status, kDeviceTimeout);
+            atomicCAS(&g_zf_device_status, kDeviceOk, kDeviceTimeout);
             return false;
         }
     }
@@ -360,13 +382,33 @@ __device__ __forceinline__ Packing tile_packing(const TileGeom& g, int n_gr) {
 
 template <int MODE, class A, class GT, bool LEAD, bool PACK>
 __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
-                              volatile int* abort_flag, uint32_t* issued_out) {
+                              volatile int* abort_flag, uint32_t* issued_out,
+                              volatile int* tile_of) {
     constexpr int NS = ModeTraits<MODE>::kStateArrays;
     constexpr int RG = GradTraits<GT>::kRanksPerStage;
+    const int slot_id = a.h.sched_slot;
+    const bool dyn = slot_id >= 0;
+    unsigned int* next_tile = dyn ? &g_zf_sched[slot_id][0] : nullptr;
     uint32_t it = 0;
-    for (int tile = blockIdx.x; tile < a.h.total_tiles; tile += gridDim.x) {
+    // Dynamic: away from the end the next claim is issued one tile ahead, so
+    // that the atomic's round trip overlaps the current tile's copies; in the
+    // last two rounds a tile is claimed only when the ring can take it, so
+    // that no CTA holds a tile back while others run dry.
+    const int total = a.h.total_tiles;
+    const int ahead_until = total - 2 * static_cast<int>(gridDim.x);
+    int tile = dyn ? static_cast<int>(atomicAdd(next_tile, 1u)) : static_cast<int>(blockIdx.x);
+    while (tile < total) {
+        int following = -1;
+        if (!dyn) {
+            following = tile + static_cast<int>(gridDim.x);
+        } else if (tile < ahead_until) {
+            following = static_cast<int>(atomicAdd(next_tile, 1u));
+        }
         const TileGeom g = tile_geom<A, GT>(a, tile);
-        if (g.nvalid == 0) continue;      // past the end of an unpadded parameter
+        if (g.nvalid == 0) {              // past the end of an unpadded parameter
+            tile = following >= 0 ? following : static_cast<int>(atomicAdd(next_tile, 1u));
+            continue;
+        }
         const int n_ranks = ModeTraits<MODE>::kReadsGrads ? g.u->n_ranks : 0;
         const uint32_t sbytes = static_cast<uint32_t>(g.state_valid) * 4;
         const uint32_t gbytes = static_cast<uint32_t>(g.a1 - g.a0) * sizeof(GT);
@@ -382,6 +424,9 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
                 stop = true;
                 break;
             }
+            // the consumers learn a dynamically claimed tile from its first
+            // stage (published before the arrive, which releases it)
+            if (st == 0) tile_of[slot] = tile;
             const int k0 = st == 0 ? 0 : r0 + (st - 1) * RG;
             const int nk = st == 0 ? r0 : min(RG, n_ranks - k0);
             const int ns = st == 0 ? NS : 0;
@@ -403,7 +448,21 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
             }
             ++it;
         }
-        if (stop || *abort_flag) break;
+        if (stop || *abort_flag) {
+            *issued_out = it;
+            return;
+        }
+        tile = following >= 0 ? following : static_cast<int>(atomicAdd(next_tile, 1u));
+    }
+    if (dyn) {
+        // No tile left: an empty stage whose tile index is -1 tells the
+        // consumers to stop.
+        const uint32_t slot = it % kStages, parity = ((it / kStages) & 1) ^ 1;
+        if (mbar_wait_bounded(smem_u32(&empty[slot]), parity, abort_flag, kWaitLimitNs)) {
+            tile_of[slot] = -1;
+            mbar_arrive(smem_u32(&full[slot]));
+            ++it;
+        }
     }
     *issued_out = it;
 }
@@ -411,7 +470,8 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
 template <int MODE, class A, class GT, bool LEAD, bool ALIGNED, bool PACK>
 __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                               uint64_t* empty, volatile int* abort_flag,
-                              unsigned int* consumed_min, float clip_coef, double* warp_sq) {
+                              unsigned int* consumed_min, float clip_coef, double* warp_sq,
+                              const volatile int* tile_of) {
     constexpr int NS = ModeTraits<MODE>::kStateArrays;
     const int tid = threadIdx.x;  // 0..kConsumers-1
     const int lane = tid & 31;
@@ -422,9 +482,31 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
     float2 sq2_s = make_float2(0.0f, 0.0f), sq2_c = make_float2(0.0f, 0.0f);
     float sq_s = 0.0f, sq_c = 0.0f;
     constexpr int RG = GradTraits<GT>::kRanksPerStage;
-    for (int tile = blockIdx.x; tile < a.h.total_tiles && ok; tile += gridDim.x) {
+    const bool dyn = a.h.sched_slot >= 0;
+    int next_static = static_cast<int>(blockIdx.x);
+    while (ok) {
+        // The next tile: in the fixed order, or (dynamic scheduling) the one
+        // the producer names in the tile's first stage, -1 when none is left.
+        const uint8_t* first_stage = nullptr;
+        int tile;
+        if (dyn) {
+            const uint32_t slot = it % kStages, parity = (it / kStages) & 1;
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(smem_u32(&full[slot]), parity,
+                                                           abort_flag, kWaitLimitNs))) {
+                ok = false;
+                break;
+            }
+            tile = tile_of[slot];
+            if (tile < 0) break;
+            first_stage = smem + slot * kStageBytes;
+        } else {
+            tile = next_static;
+            if (tile >= a.h.total_tiles) break;
+            next_static += static_cast<int>(gridDim.x);
+        }
         const TileGeom g = tile_geom<A, GT>(a, tile);
-        if (g.nvalid == 0) continue;      // past the end of an unpadded parameter (uniform)
+        if (g.nvalid == 0) continue;      // past the end of an unpadded parameter (uniform;
+                                          // a dynamic producer never names such a tile)
         const UnitDesc* u = g.u;
         const int n_ranks = u->n_ranks;
         const int first = tid * kVec;
@@ -534,7 +616,7 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
         const Packing pk = tile_packing<MODE, GT, LEAD, PACK>(g, n_gr);
         const int r0 = pk.on ? n_gr : lead_ranks<NS, GT, LEAD>(n_gr);
         {
-            const uint8_t* stage = wait_full();
+            const uint8_t* stage = first_stage != nullptr ? first_stage : wait_full();
             if (stage == nullptr) {
                 ok = false;
                 continue;
@@ -731,6 +813,7 @@ staged_step_kernel(const __grid_constant__ A a) {
     __shared__ unsigned int consumed_min;
     __shared__ float clip_coef;
     __shared__ double warp_sq[kConsumerWarps];
+    __shared__ int tile_of[kStages];
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
             mbar_init(smem_u32(&full[i]), 1);
@@ -768,11 +851,13 @@ staged_step_kernel(const __grid_constant__ A a) {
     __syncthreads();
     if (threadIdx.x >= kConsumers) {
         if (threadIdx.x == kConsumers) {
-            producer_loop<MODE, A, GT, LEAD, PACK>(a, smem, full, empty, &abort_flag, &issued);
+            producer_loop<MODE, A, GT, LEAD, PACK>(a, smem, full, empty, &abort_flag, &issued,
+                                                   tile_of);
         }
     } else {
         consumer_loop<MODE, A, GT, LEAD, ALIGNED, PACK>(a, smem, full, empty, &abort_flag,
-                                                  &consumed_min, clip_coef, warp_sq);
+                                                        &consumed_min, clip_coef, warp_sq,
+                                                        tile_of);
     }
     __syncthreads();
     if constexpr (ModeTraits<MODE>::kNorm) {
@@ -788,6 +873,23 @@ staged_step_kernel(const __grid_constant__ A a) {
             const uint32_t slot = it % kStages, parity = (it / kStages) & 1;
             int dummy = 0;
             mbar_wait_bounded(smem_u32(&full[slot]), parity, &dummy, kDrainLimitNs);
+        }
+    }
+    if (threadIdx.x == 0 && a.h.sched_slot >= 0) {
+        // Every claim of this CTA came before the barrier above; the last CTA
+        // to get here puts the scheduling slot back to zero for the next
+        // launch.  Each CTA claims every tile it takes plus one past the end,
+        // so a slot used by this launch alone ends at total_tiles + gridDim.x;
+        // anything else means another launch claimed from it meanwhile (an
+        // aborted launch has recorded its timeout already).
+        unsigned int* sl = g_zf_sched[a.h.sched_slot];
+        __threadfence();
+        if (atomicAdd(&sl[1], 1u) == gridDim.x - 1) {
+            const unsigned int claims = atomicExch(&sl[0], 0u);
+            atomicExch(&sl[1], 0u);
+            if (claims != static_cast<unsigned int>(a.h.total_tiles) + gridDim.x) {
+                atomicCAS(&g_zf_device_status, kDeviceOk, kDeviceSchedConflict);
+            }
         }
     }
 }
@@ -855,13 +957,15 @@ static cudaError_t launch_form(const MultiArgs& a, int n_ptrs, cudaStream_t stre
 }
 
 // Pick the kernel form: LEAD when every unit's whole tile fits one stage, the
-// ALIGNED form of the fused step when every unit's S is a multiple of 8.
+// ALIGNED form when every unit's S is a multiple of 8; and
+// the tile order (a.h.sched_slot).
 template <int MODE, class GT = uint16_t>
-static cudaError_t launch_sized(const MultiArgs& a, int n_ptrs, cudaStream_t stream) {
+static cudaError_t launch_sized(MultiArgs& a, int n_ptrs, cudaStream_t stream) {
     constexpr int NS = ModeTraits<MODE>::kStateArrays;
     constexpr bool kCanLead = can_lead<NS, GT>() && ModeTraits<MODE>::kReadsGrads;
-    constexpr bool kHasAligned =
-        sizeof(GT) == 2 && (MODE == kModePlain || MODE == kModeAccumFinal);
+    // every bf16-gradient mode has an ALIGNED form (the clipped step's norm
+    // and update passes measured 2.5 % faster with it on GPT-2-small)
+    constexpr bool kHasAligned = sizeof(GT) == 2;
     int max_ranks = 0;
     bool aligned = true;
     for (int i = 0; i < a.h.n_units; ++i) {
@@ -869,6 +973,21 @@ static cudaError_t launch_sized(const MultiArgs& a, int n_ptrs, cudaStream_t str
         if (a.unit[i].S % 8 != 0) aligned = false;
     }
     const bool lead = kCanLead && max_ranks <= first_stage_ranks<GT>(NS);
+    // Dynamic tile order for launches whose tiles take one stage each and that
+    // run many rounds of tiles: there the SMs' speeds differ (measured on
+    // GB300: up to 40 %) and a fixed order leaves the fast ones idle at the
+    // end.  Launches of multi-stage tiles are bound by DRAM as a whole and
+    // keep every SM equally busy; short launches (few rounds) measured slower
+    // with the claims.  The norm passes keep the fixed order so that their
+    // per-CTA partial sums, and the norm, are reproducible bit for bit.
+    constexpr int RG = GradTraits<GT>::kRanksPerStage;
+    const bool one_stage = !ModeTraits<MODE>::kReadsGrads || lead ||
+                           (NS == 0 && max_ranks <= RG);
+    a.h.sched_slot = -1;
+    if (!ModeTraits<MODE>::kNorm && one_stage && a.h.grid == 0 &&
+        a.h.total_tiles >= kDynamicMinRounds * grid_for<MODE, MultiArgsS>(a.h.total_tiles)) {
+        a.h.sched_slot = sched_slot(stream);
+    }
     if constexpr (kHasAligned) {
         if (aligned) {
             if constexpr (kCanLead) {
@@ -891,9 +1010,57 @@ static cudaError_t launch_sized(const MultiArgs& a, int n_ptrs, cudaStream_t str
     return launch_form<MODE, GT, false, false>(a, n_ptrs, stream);
 }
 
-cudaError_t launch_staged_step_f32(const MultiArgs& a, int n_ptrs, cudaStream_t stream) {
+cudaError_t launch_staged_step_f32(MultiArgs& a, int n_ptrs, cudaStream_t stream) {
     if (a.h.total_tiles <= 0) return cudaSuccess;
     return launch_sized<kModeMeanDiv, float>(a, n_ptrs, stream);
+}
+
+// Scheduling slot of a launch on `stream` on the current device.  Launches
+// made directly get their stream's slot, one per (device, stream): a stream
+// runs its launches one after another and each launch leaves its slot at
+// zero, so launches sharing a slot never overlap.  Launches captured into a
+// CUDA graph take the capture slots in turn (a replay runs in whatever stream
+// the graph is launched into).  -1 (the fixed order) once the stream slots
+// are used up or when the stream's state cannot be read.  Two launches
+// running at once on one slot -- a stream destroyed with a launch still
+// running and its handle handed out again, or graphs holding more than
+// kSharedSlot - kStreamSlots captured launches replayed at once -- are
+// detected at the end of the launch (ZERO_DEVICE_SCHED_CONFLICT).
+int sched_slot(cudaStream_t stream) {
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(stream, &cap) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return -1;
+    }
+    if (dev < 0 || dev >= 64) return -1;
+    if (const char* f = std::getenv("ZERO_SCHED_SHARED")) {
+        // failure injection for tests: every launch on one slot of its own
+        if (f[0] != '\0' && f[0] != '0') return kSharedSlot;
+    }
+    struct Key {
+        int dev;
+        cudaStream_t stream;
+        int slot;
+    };
+    static std::mutex mu;
+    static std::vector<Key> keys;
+    static int used[64] = {};
+    static unsigned int captured[64] = {};
+    std::lock_guard<std::mutex> lock(mu);
+    if (cap != cudaStreamCaptureStatusNone) {
+        return kStreamSlots + static_cast<int>(captured[dev]++ % (kSharedSlot - kStreamSlots));
+    }
+    for (const Key& k : keys) {
+        if (k.dev == dev && k.stream == stream) return k.slot;
+    }
+    if (used[dev] >= kStreamSlots) return -1;
+    keys.push_back(Key{dev, stream, used[dev]++});
+    return keys.back().slot;
 }
 
 int staged_grid(int mode, int total_tiles) {
@@ -903,7 +1070,7 @@ int staged_grid(int mode, int total_tiles) {
     return grid_for<kModePlain, MultiArgsS>(total_tiles);
 }
 
-cudaError_t launch_staged_step(const MultiArgs& a, int n_ptrs, int mode, cudaStream_t stream) {
+cudaError_t launch_staged_step(MultiArgs& a, int n_ptrs, int mode, cudaStream_t stream) {
     if (a.h.total_tiles <= 0) return cudaSuccess;
     switch (mode) {
         case kModePlain: return launch_sized<kModePlain>(a, n_ptrs, stream);

@@ -260,12 +260,14 @@ def zero_step(grads, master, m, v, accum, micro_step: int, n_micro: int, full_pa
 
 ZERO_DEVICE_OK = 0
 ZERO_DEVICE_TIMEOUT = 1
+ZERO_DEVICE_SCHED_CONFLICT = 2
 
 
 def zero_device_status(stream=None, clear: bool = True) -> int:
     """Synchronise the stream and return (and by default clear) the device
-    status word: ZERO_DEVICE_OK, or ZERO_DEVICE_TIMEOUT if a kernel's bounded
-    wait ran out."""
+    status word: ZERO_DEVICE_OK, ZERO_DEVICE_TIMEOUT if a kernel's bounded
+    wait ran out, or ZERO_DEVICE_SCHED_CONFLICT if two launches claimed tiles
+    from one scheduling counter at the same time."""
     v = ctypes.c_int32(0)
     _check(load().zero_device_status(_stream(stream), ctypes.byref(v), int(bool(clear))),
            "zero_device_status")

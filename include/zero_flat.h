@@ -25,9 +25,23 @@
  *   - bf16 values travel as uint16_t bit patterns; fp32 as float.
  *   - Every buffer is owned by the caller.  The library allocates no memory
  *     and keeps no state between calls except one device status word (see
- *     zero_device_status) and the 32 KB scratch array of
- *     zero_step_units_clip_noalloc; only zero_device_status synchronises a
- *     stream.
+ *     zero_device_status), the 32 KB scratch array of
+ *     zero_step_units_clip_noalloc and 16 KB of tile-scheduling counters;
+ *     only zero_device_status synchronises a stream.
+ *   - Tile scheduling: the fused kernels stream tiles of 4096 elements of one
+ *     rank's shard through persistent CTAs, one per SM.  When every tile of a
+ *     launch takes one pass through the kernel's shared-memory ring (N_d <= 2
+ *     for the plain step; the update pass of the clipped step) and the launch
+ *     runs at least 16 rounds of tiles, the CTAs claim tiles from a counter
+ *     instead of taking them in a fixed order, so that faster SMs take more
+ *     (the SMs' speeds differ by up to 40 % there).  Results do not depend on
+ *     the order.  Launches made directly use a counter per (device, stream);
+ *     launches captured into a CUDA graph take one of 1023 capture counters
+ *     in turn.  Each launch leaves its counter at zero; if two launches ever
+ *     claim from one counter at the same time (a stream destroyed while its
+ *     last launch runs and its handle reused at once, or more than 1023
+ *     captured launches replayed concurrently), their results are wrong and
+ *     ZERO_DEVICE_SCHED_CONFLICT is recorded (see zero_device_status).
  *   - Device-side calls are asynchronous on `stream` (a cudaStream_t, or NULL
  *     for the legacy default stream) and return after the launch.  The return
  *     code covers argument checks and launch errors; completion and any later
@@ -50,6 +64,10 @@
  *     queuing some of them.  zero_last_error() gives a message (per calling
  *     thread).
  *   - Failure injection, for tests of callers' error paths: while the
+ *     environment variable ZERO_SCHED_SHARED is set (to anything but "0"),
+ *     every dynamically scheduled launch claims its tiles from one counter
+ *     kept for this purpose, so that launches on two streams at once collide.
+ *     While the
  *     environment variable ZERO_INJECT_FAILURE is set, every CUDA call the
  *     library would make whose label contains its value (for example
  *     "clip update pass", "staged launch", "gradient copy to the device") is
@@ -252,13 +270,17 @@ int zero_step(const uint16_t* const* grads, float* const* master, float* const* 
  * that wait on shared-memory barriers (the bulk-copy staged fused step and
  * reduce-scatter): every such wait gives up after about 2 seconds, records
  * ZERO_DEVICE_TIMEOUT in a device status word, and the kernel returns early
- * (its outputs are then incomplete).  This call synchronises `stream`, stores
- * the word in *status (ZERO_DEVICE_OK when nothing went wrong) and, if clear
- * != 0, resets it.  No counterpart on the pages: it reports a launch that did
- * not complete, instead of letting a wait hang the GPU.
+ * (its outputs are then incomplete).  A dynamically scheduled launch that
+ * found its tile counter used by another launch at the same time records
+ * ZERO_DEVICE_SCHED_CONFLICT (its outputs are wrong; see "Tile scheduling"
+ * above).  The first problem recorded stays.  This call synchronises
+ * `stream`, stores the word in *status (ZERO_DEVICE_OK when nothing went
+ * wrong) and, if clear != 0, resets it.  No counterpart on the pages: it
+ * reports a launch that did not complete, instead of letting a wait hang the
+ * GPU.
  * Errors: ZERO_ERR_INVALID_ARG (status NULL), ZERO_ERR_CUDA.
  */
-enum { ZERO_DEVICE_OK = 0, ZERO_DEVICE_TIMEOUT = 1 };
+enum { ZERO_DEVICE_OK = 0, ZERO_DEVICE_TIMEOUT = 1, ZERO_DEVICE_SCHED_CONFLICT = 2 };
 int zero_device_status(void* stream, int32_t* status, int32_t clear);
 
 /*

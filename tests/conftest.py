@@ -58,7 +58,8 @@ def pytest_terminal_summary(terminalreporter):
     for rec in parity.MARGINS:
         key = (rec["test"], rec["kind"], rec["what"])
         a = agg.setdefault(key, dict(n=0, checks=0, max_rel=0.0, max_ulp=0, exact=1.0,
-                                     floor_only=0, max_over_tol=0.0))
+                                     floor_only=0, max_over_tol=0.0, floor_only_max_ulp=0,
+                                     floor_only_max_abs_ref=0.0))
         a["checks"] += 1
         a["n"] += rec["n"]
         a["max_rel"] = max(a["max_rel"], rec.get("max_rel", 0.0))
@@ -66,6 +67,9 @@ def pytest_terminal_summary(terminalreporter):
         a["exact"] = min(a["exact"], rec["exact"])
         a["floor_only"] += rec.get("floor_only", 0)
         a["max_over_tol"] = max(a["max_over_tol"], rec.get("max_over_tol", 0.0))
+        a["floor_only_max_ulp"] = max(a["floor_only_max_ulp"], rec.get("floor_only_max_ulp", 0))
+        a["floor_only_max_abs_ref"] = max(a["floor_only_max_abs_ref"],
+                                          rec.get("floor_only_max_abs_ref", 0.0))
     tr = terminalreporter
     tr.write_sep("=", "parity margins (worst over each test's checks)")
     tr.write_line(f"{'test':60s} {'array':8s} {'elements':>11s} {'max rel':>9s} "
@@ -77,14 +81,19 @@ def pytest_terminal_summary(terminalreporter):
                       f"{a['max_over_tol']:6.3f}")
     tot = {}
     for (test, kind, what), a in agg.items():
-        t = tot.setdefault(what, dict(n=0, max_rel=0.0, max_ulp=0, exact=1.0, floor_only=0))
+        t = tot.setdefault(what, dict(n=0, max_rel=0.0, max_ulp=0, exact=1.0, floor_only=0,
+                                      max_over_tol=0.0, floor_only_max_ulp=0,
+                                      floor_only_max_abs_ref=0.0))
         t["n"] += a["n"]
-        t["max_rel"] = max(t["max_rel"], a["max_rel"])
-        t["max_ulp"] = max(t["max_ulp"], a["max_ulp"])
+        for k in ("max_rel", "max_ulp", "max_over_tol", "floor_only_max_ulp",
+                  "floor_only_max_abs_ref"):
+            t[k] = max(t[k], a[k])
         t["exact"] = min(t["exact"], a["exact"])
         t["floor_only"] += a["floor_only"]
-    tr.write_sep("-", "all tests")
+    tr.write_sep("-", "all tests (max rel and max ulp: where the relative criterion binds)")
     for what, t in sorted(tot.items()):
         tr.write_line(f"{what:8s} elements {t['n']:d}  max rel {t['max_rel']:.2e}  "
                       f"max ulp {t['max_ulp']}  min exact {t['exact']:.6f}  "
-                      f"floor-only {t['floor_only']}")
+                      f"max d/tol {t['max_over_tol']:.3f}  floor-only {t['floor_only']} "
+                      f"(max ulp {t['floor_only_max_ulp']}, |ref| <= "
+                      f"{t['floor_only_max_abs_ref']:.2e})")

@@ -64,12 +64,15 @@ def check_state(name, got, ref, floor_scale=None):
         floor = 1e-7 * scale
     tol = 1e-6 * np.abs(ref) + floor
     d = np.abs(got - ref)
-    nz = ref != 0
-    _record("state", name, n=int(ref.size),
-            max_rel=float(np.max(d[nz] / np.abs(ref[nz]))) if nz.any() else 0.0,
+    # relative regime: elements where 1e-6 |ref| is at least the floor
+    rel = 1e-6 * np.abs(ref) >= floor
+    _record("state", name, n=int(ref.size), n_relative=int(np.count_nonzero(rel)),
+            max_rel=float(np.max(d[rel] / np.abs(ref[rel]))) if rel.any() else 0.0,
+            max_f32_ulp=_max_f32_ulp(got[rel], ref[rel]),
+            max_abs_below_floor=float(np.max(d[~rel])) if (~rel).any() else 0.0,
             max_over_tol=float(np.max(d / np.maximum(tol, 1e-300))) if ref.size else 0.0,
             floor_only=int(np.count_nonzero((d > 1e-6 * np.abs(ref)) & (d <= tol))),
-            max_f32_ulp=_max_f32_ulp(got, ref), exact=_exact_fraction(got, ref))
+            exact=_exact_fraction(got, ref))
     bad = np.nonzero(~(d <= tol))[0]
     assert bad.size == 0, f"{name}: {bad.size}/{ref.size} out of tolerance; " + \
         _fmt(bad[0], got[bad[0]], ref[bad[0]])
@@ -121,10 +124,15 @@ def check_bf16(got_bits, ref_bits, what="params", min_exact=0.999):
     d = np.abs(bf16_value(got_bits) - bf16_value(ref_bits))
     ulp = bf16_ulp(ref_bits)
     tol = ulp + 1e-7
+    dist = np.abs(bf16_ordered(got_bits) - bf16_ordered(ref_bits)) if got_bits.size else \
+        np.zeros(0, np.int64)
+    floor_only = (d > ulp) & (d <= tol)
     _record("bf16", what, n=int(ref_bits.size),
-            max_ulp=int(np.max(np.abs(bf16_ordered(got_bits) - bf16_ordered(ref_bits))))
-            if got_bits.size else 0,
-            floor_only=int(np.count_nonzero((d > ulp) & (d <= tol))),
+            max_ulp=int(np.max(dist[~floor_only])) if (~floor_only).any() else 0,
+            floor_only=int(np.count_nonzero(floor_only)),
+            floor_only_max_ulp=int(np.max(dist[floor_only])) if floor_only.any() else 0,
+            floor_only_max_abs_ref=float(np.max(np.abs(bf16_value(ref_bits)[floor_only])))
+            if floor_only.any() else 0.0,
             exact=float(np.mean(got_bits == ref_bits)) if got_bits.size else 1.0)
     bad = np.nonzero(d > tol)[0]
     assert bad.size == 0, f"{what}: {bad.size} bf16 values out of tolerance; " + \

@@ -1,0 +1,159 @@
+"""Dynamic tile order of the staged kernel.
+
+Launches whose tiles take one pass through the shared-memory ring (N_d <= 2,
+the clipped step's update pass) and that run many rounds of tiles let the CTAs
+claim tiles from a counter.  The results must not depend on the order: the
+same bits as the direct-load kernels (fixed order), eagerly, replayed from a
+CUDA graph, and on two streams at once.  Two launches forced onto one counter
+at the same time must never corrupt results silently: wrong bits come with
+ZERO_DEVICE_SCHED_CONFLICT.
+"""
+import pytest
+import torch
+
+from gpu_harness import hp_at
+
+import fsdp_sharded_mixed_flatten_gb300 as zf
+from fsdp_sharded_mixed_flatten_gb300 import synthetic
+from fsdp_sharded_mixed_flatten_gb300.buffers import FlatUnit
+
+pytestmark = pytest.mark.gpu
+
+# N_d = 2 with S mod 8 = 7: ceil(S / 4096) * 2 = 4884 tiles, over 16 rounds of
+# 152 CTAs, so the launch is dynamically scheduled (LEAD form)
+BIG_N2 = ([20_000_013], 2)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _gpu():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from fsdp_sharded_mixed_flatten_gb300 import build
+    build.build()
+    zf.load()
+
+
+def _unit(spec, tag, accum=False):
+    numels, n = spec
+    u = FlatUnit(numels, n, accum=accum)
+    u.set_master_flat(synthetic.make_master_flat(u.P, n, 0.02, (tag,)).cuda())
+    return u
+
+
+def _grads(u, t, tag):
+    return synthetic.make_grads(u.P, u.n_ranks, 1e-2, (tag, t)).cuda()
+
+
+def _bits(u):
+    return [x.contiguous().view(torch.int32).clone() for x in (u.master, u.m, u.v)] + \
+        [u.params.contiguous().view(torch.int16).clone()]
+
+
+def _same(a, b):
+    return all(torch.equal(x, y) for x, y in zip(a, b))
+
+
+def _step(u, t, stream=None):
+    zf.zero_step(u.grad_rows(), *u.state_rows(), None, 1, 1, u.param_rows(), u.layout, hp_at(t),
+                 stream=stream)
+
+
+def test_dynamic_order_equals_fixed_order(monkeypatch):
+    """The staged kernel (dynamic order here) against the direct-load kernels
+    (fixed order), 3 steps, bit for bit."""
+    runs = {}
+    for kern in ("staged", "direct"):
+        if kern == "direct":
+            monkeypatch.setenv("ZERO_STEP_KERNEL", "direct")
+        else:
+            monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
+        u = _unit(BIG_N2, "dyn-vs-fixed")
+        for t in (1, 2, 3):
+            u.grads.copy_(_grads(u, t, "dyn-vs-fixed"))
+            _step(u, t)
+        torch.cuda.synchronize()
+        runs[kern] = _bits(u)
+    monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
+    assert _same(runs["staged"], runs["direct"])
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
+def test_graph_replay_equals_eager():
+    """Steps captured into a CUDA graph (capture counters) and replayed twice
+    give the bits of the same steps run eagerly."""
+    a, b = _unit(BIG_N2, "graph"), _unit(BIG_N2, "graph")
+    g = _grads(a, 1, "graph")
+    a.grads.copy_(g)
+    b.grads.copy_(g)
+    _step(a, 1)                       # warm-up outside capture (kernel attributes)
+    _step(b, 1)
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for t in (2, 3):
+            _step(a, t)
+    for _ in range(2):
+        graph.replay()
+    torch.cuda.synchronize()
+    for _ in range(2):
+        for t in (2, 3):
+            _step(b, t)
+    torch.cuda.synchronize()
+    assert _same(_bits(a), _bits(b))
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
+def test_two_streams_at_once_equal_one_after_the_other():
+    """Dynamically scheduled launches on two streams at once (each stream has
+    its own counter) equal the same launches run one after the other."""
+    specs = [BIG_N2, ([12_000_001], 1)]
+    conc = [_unit(s, f"two-streams-{i}") for i, s in enumerate(specs)]
+    seq = [_unit(s, f"two-streams-{i}") for i, s in enumerate(specs)]
+    grads = [[_grads(u, t, f"ts{i}") for t in (1, 2, 3)] for i, u in enumerate(conc)]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for t in (1, 2, 3):
+        for u, s, g in zip(conc, streams, grads):
+            with torch.cuda.stream(s):
+                u.grads.copy_(g[t - 1])
+                _step(u, t, stream=s)
+    torch.cuda.synchronize()
+    for t in (1, 2, 3):
+        for u, g in zip(seq, grads):
+            u.grads.copy_(g[t - 1])
+            _step(u, t)
+    torch.cuda.synchronize()
+    for a, b in zip(conc, seq):
+        assert _same(_bits(a), _bits(b))
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
+def test_shared_counter_conflict_is_reported(monkeypatch):
+    """Failure injection: with ZERO_SCHED_SHARED every dynamic launch claims
+    from one counter, so launches on two streams at once may take tiles from
+    each other.  Wrong results then always come with ZERO_DEVICE_SCHED_CONFLICT
+    (never silently); launches that did not overlap are right.  No wait is
+    involved: every launch ends."""
+    monkeypatch.setenv("ZERO_SCHED_SHARED", "1")
+    specs = [BIG_N2, ([12_000_007], 2)]
+    conc = [_unit(s, f"conflict-{i}") for i, s in enumerate(specs)]
+    ref = [_unit(s, f"conflict-{i}") for i, s in enumerate(specs)]
+    grads = [_grads(u, 1, f"cf{i}") for i, u in enumerate(conc)]
+    for u, g in zip(conc + ref, grads + grads):
+        u.grads.copy_(g)
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for u, s in zip(conc, streams):
+        with torch.cuda.stream(s):
+            _step(u, 1, stream=s)
+    torch.cuda.synchronize()
+    status = zf.zero_device_status()
+    monkeypatch.delenv("ZERO_SCHED_SHARED", raising=False)
+    for u in ref:                      # one after the other, each on its own stream's counter
+        _step(u, 1)
+    torch.cuda.synchronize()
+    right = all(_same(_bits(a), _bits(b)) for a, b in zip(conc, ref))
+    assert status in (zf.zero.ZERO_DEVICE_OK, zf.zero.ZERO_DEVICE_SCHED_CONFLICT)
+    if not right:
+        assert status == zf.zero.ZERO_DEVICE_SCHED_CONFLICT
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
