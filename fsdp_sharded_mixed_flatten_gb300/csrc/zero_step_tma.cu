@@ -44,11 +44,12 @@ namespace zf {
 
 __device__ int g_zf_device_status = 0;
 
-// Dynamic tile scheduling.  The persistent CTAs of a launch claim tiles from
-// one counter instead of striding through them in a fixed order: measured on
-// GB300, the SMs of a launch whose tiles take one stage each (N_d <= 2, the
-// clipped step's update pass) run at speeds up to 40 % apart, and with a fixed
-// order the fast ones sat idle for the last 15 % of the launch.  Every
+// Dynamic tile scheduling.  The persistent CTAs of a long launch claim tiles
+// from one counter instead of striding through them in a fixed order:
+// measured on GB300, the SMs of a launch whose tiles take one stage each
+// (N_d <= 2, the clipped step's update pass) run at speeds up to 40 % apart,
+// and with a fixed order the fast ones sat idle for the last 15 % of the
+// launch; launches of multi-stage tiles gained 1-2 % as well.  Every
 // element's result is the same whichever CTA computes it.  A slot is
 // {next tile, CTAs finished}; the last CTA of a launch to finish puts it back
 // to zero, so the slot is ready for the next launch on the same stream (the
@@ -390,23 +391,21 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
     const bool dyn = slot_id >= 0;
     unsigned int* next_tile = dyn ? &g_zf_sched[slot_id][0] : nullptr;
     uint32_t it = 0;
-    // Dynamic: away from the end the next claim is issued one tile ahead, so
-    // that the atomic's round trip overlaps the current tile's copies; in the
-    // last two rounds a tile is claimed only when the ring can take it, so
-    // that no CTA holds a tile back while others run dry.
+    // Every CTA's first tile is its own index.  After it, in the fixed order,
+    // CTA c takes c + G, c + 2G, ...; in the dynamic order it claims the next
+    // tile (G + the counter) when its ring has room for it: the ring runs
+    // ahead of the consumers, so the claim's round trip overlaps their work,
+    // and no CTA holds a tile back while others run dry.
     const int total = a.h.total_tiles;
-    const int ahead_until = total - 2 * static_cast<int>(gridDim.x);
-    int tile = dyn ? static_cast<int>(atomicAdd(next_tile, 1u)) : static_cast<int>(blockIdx.x);
+    const int G = static_cast<int>(gridDim.x);
+    auto next_of = [&](int t) -> int {
+        return dyn ? G + static_cast<int>(atomicAdd(next_tile, 1u)) : t + G;
+    };
+    int tile = static_cast<int>(blockIdx.x);
     while (tile < total) {
-        int following = -1;
-        if (!dyn) {
-            following = tile + static_cast<int>(gridDim.x);
-        } else if (tile < ahead_until) {
-            following = static_cast<int>(atomicAdd(next_tile, 1u));
-        }
         const TileGeom g = tile_geom<A, GT>(a, tile);
         if (g.nvalid == 0) {              // past the end of an unpadded parameter
-            tile = following >= 0 ? following : static_cast<int>(atomicAdd(next_tile, 1u));
+            tile = next_of(tile);
             continue;
         }
         const int n_ranks = ModeTraits<MODE>::kReadsGrads ? g.u->n_ranks : 0;
@@ -452,7 +451,7 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
             *issued_out = it;
             return;
         }
-        tile = following >= 0 ? following : static_cast<int>(atomicAdd(next_tile, 1u));
+        tile = next_of(tile);
     }
     if (dyn) {
         // No tile left: an empty stage whose tile index is -1 tells the
@@ -878,8 +877,9 @@ staged_step_kernel(const __grid_constant__ A a) {
     if (threadIdx.x == 0 && a.h.sched_slot >= 0) {
         // Every claim of this CTA came before the barrier above; the last CTA
         // to get here puts the scheduling slot back to zero for the next
-        // launch.  Each CTA claims every tile it takes plus one past the end,
-        // so a slot used by this launch alone ends at total_tiles + gridDim.x;
+        // launch.  The counter hands out tiles G, G + 1, ... and every CTA
+        // makes one claim past the end, so a slot used by this launch alone
+        // ends at total_tiles (a dynamic launch has total_tiles >= G);
         // anything else means another launch claimed from it meanwhile (an
         // aborted launch has recorded its timeout already).
         unsigned int* sl = g_zf_sched[a.h.sched_slot];
@@ -887,7 +887,7 @@ staged_step_kernel(const __grid_constant__ A a) {
         if (atomicAdd(&sl[1], 1u) == gridDim.x - 1) {
             const unsigned int claims = atomicExch(&sl[0], 0u);
             atomicExch(&sl[1], 0u);
-            if (claims != static_cast<unsigned int>(a.h.total_tiles) + gridDim.x) {
+            if (claims != static_cast<unsigned int>(a.h.total_tiles)) {
                 atomicCAS(&g_zf_device_status, kDeviceOk, kDeviceSchedConflict);
             }
         }
@@ -973,18 +973,15 @@ static cudaError_t launch_sized(MultiArgs& a, int n_ptrs, cudaStream_t stream) {
         if (a.unit[i].S % 8 != 0) aligned = false;
     }
     const bool lead = kCanLead && max_ranks <= first_stage_ranks<GT>(NS);
-    // Dynamic tile order for launches whose tiles take one stage each and that
-    // run many rounds of tiles: there the SMs' speeds differ (measured on
-    // GB300: up to 40 %) and a fixed order leaves the fast ones idle at the
-    // end.  Launches of multi-stage tiles are bound by DRAM as a whole and
-    // keep every SM equally busy; short launches (few rounds) measured slower
-    // with the claims.  The norm passes keep the fixed order so that their
-    // per-CTA partial sums, and the norm, are reproducible bit for bit.
-    constexpr int RG = GradTraits<GT>::kRanksPerStage;
-    const bool one_stage = !ModeTraits<MODE>::kReadsGrads || lead ||
-                           (NS == 0 && max_ranks <= RG);
+    // Dynamic tile order for launches that run many rounds of tiles: the SMs'
+    // speeds differ (measured on GB300: up to 40 % where a tile takes one
+    // stage) and a fixed order leaves the fast ones idle at the end.  Short
+    // launches (fewer than kDynamicMinRounds rounds) measured about 1 % slower
+    // with the claims and keep the fixed order.  The norm passes keep it too,
+    // so that their per-CTA partial sums, and the norm, are reproducible bit
+    // for bit.
     a.h.sched_slot = -1;
-    if (!ModeTraits<MODE>::kNorm && one_stage && a.h.grid == 0 &&
+    if (!ModeTraits<MODE>::kNorm && a.h.grid == 0 &&
         a.h.total_tiles >= kDynamicMinRounds * grid_for<MODE, MultiArgsS>(a.h.total_tiles)) {
         a.h.sched_slot = sched_slot(stream);
     }

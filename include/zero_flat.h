@@ -29,13 +29,13 @@
  *     zero_step_units_clip_noalloc and 16 KB of tile-scheduling counters;
  *     only zero_device_status synchronises a stream.
  *   - Tile scheduling: the fused kernels stream tiles of 4096 elements of one
- *     rank's shard through persistent CTAs, one per SM.  When every tile of a
- *     launch takes one pass through the kernel's shared-memory ring (N_d <= 2
- *     for the plain step; the update pass of the clipped step) and the launch
- *     runs at least 16 rounds of tiles, the CTAs claim tiles from a counter
- *     instead of taking them in a fixed order, so that faster SMs take more
- *     (the SMs' speeds differ by up to 40 % there).  Results do not depend on
- *     the order.  Launches made directly use a counter per (device, stream);
+ *     rank's shard through persistent CTAs, one per SM.  When a launch runs
+ *     at least 16 rounds of tiles (and is not a norm pass of the clipped
+ *     step), each CTA takes its first tile by its index and then claims tiles
+ *     from a counter instead of taking them in a fixed order, so that faster
+ *     SMs take more (the SMs' speeds differ by up to 40 % when a tile takes
+ *     one pass through the kernel's shared-memory ring).  Results do not
+ *     depend on the order.  Launches made directly use a counter per (device, stream);
  *     launches captured into a CUDA graph take one of 1023 capture counters
  *     in turn.  Each launch leaves its counter at zero; if two launches ever
  *     claim from one counter at the same time (a stream destroyed while its
