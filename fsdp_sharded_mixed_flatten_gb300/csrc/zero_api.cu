@@ -284,7 +284,12 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
         const int n = u.L->n_ranks;
         const int need = pointers_needed(u, mode);
         const int64_t tpr = (u.L->shard_numel + zf::kStagedTile - 1) / zf::kStagedTile;
-        const int64_t tiles = tpr * n;
+        // the fused step takes every rank's last piece of at most 8 elements as
+        // one tile (the unit's tail group) instead of one tile per rank
+        const int64_t tail = u.L->shard_numel % zf::kStagedTile;
+        const bool group = mode == zf::kModePlain && tail > 0 && tail <= zf::kTailGroupMax &&
+                           n <= zf::kMaxRanks;
+        const int64_t tiles = group ? (tpr - 1) * n + 1 : tpr * n;
         if (a.h.n_units == zf::kMaxUnits || np + need > zf::kMaxPtrs ||
             static_cast<int64_t>(a.h.total_tiles) + tiles > std::numeric_limits<int32_t>::max()) {
             if (int rc = flush()) return rc;
@@ -300,6 +305,7 @@ int launch_units_staged(const UnitView* units, int n_units, int mode, const zf::
         d.n_ranks_f = static_cast<float>(n);
         d.inv_n = static_cast<float>(1.0 / static_cast<double>(n));
         d.n_pow2 = (n & (n - 1)) == 0 ? 1 : 0;
+        d.tail_group = group ? 1 : 0;
         d.off_grads = d.off_master = d.off_m = d.off_v = d.off_accum = d.off_out = -1;
         if (mode_reads_grads(mode)) {
             d.off_grads = np;

@@ -89,7 +89,10 @@ struct UnitDesc {
     float n_ranks_f;
     float inv_n;
     int32_t n_pow2;
+    int32_t tail_group;       // fused step with S mod kStagedTile in [1, kTailGroupMax]: every
+                              // rank's last piece in one tile (the unit's last)
 };
+constexpr int kTailGroupMax = 8;   // elements per rank in a tail group (one thread's group)
 
 // Launch-wide fields of a staged launch.
 struct MultiHeader {

@@ -108,6 +108,9 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;       // 2 s
 constexpr uint64_t kDrainLimitNs = 200000000ull;       // 0.2 s
 
 static_assert(kConsumers * kVec == kStagedTile, "one thread owns 8 elements of a tile");
+static_assert(kConsumers >= kMaxRanks && kTailGroupMax <= kVec && kMaxUnits <= 64,
+              "a tail group gives every rank one consumer thread and one group of elements; "
+              "a 64-bit mask names a launch's units");
 static_assert(4 * kStateArrayBytes <= kStageBytes, "the state arrays must fit one stage");
 
 // Ranks whose gradient slices share the first stage of a tile with its NS
@@ -231,6 +234,7 @@ struct TileGeom {
     int64_t a0;       // aligned start of every rank's copied slice
     int64_t a1;       // end of the copied slice (aligned, never past the last full 16 bytes)
     int state_valid;  // state elements copied (multiple of 4)
+    bool group;       // the unit's tail group: every rank's short last piece (tail_group)
 };
 
 template <class A, class GT>
@@ -246,6 +250,20 @@ __device__ __forceinline__ TileGeom tile_geom(const A& a, int tile) {
     // the last round of the persistent CTAs instead of lengthening it.
     const int full = static_cast<int>(S / kStagedTile);
     const int n_full = full * g.u->n_ranks;
+    g.group = false;
+    if (local >= n_full && g.u->tail_group) {
+        // One tile for every rank's last S mod 4096 (<= 8) elements: no stage
+        // carries it; consumer thread r computes rank r's piece (tail_group).
+        g.group = true;
+        g.r = 0;
+        g.j0 = static_cast<int64_t>(full) * kStagedTile;
+        g.nvalid = g.u->n_ranks;
+        g.e0 = g.j0;
+        g.mis = 0;
+        g.a0 = g.a1 = 0;
+        g.state_valid = 0;
+        return g;
+    }
     if (local < n_full) {
         g.r = local / full;
         g.j0 = static_cast<int64_t>(local - g.r * full) * kStagedTile;
@@ -381,6 +399,92 @@ __device__ __forceinline__ Packing tile_packing(const TileGeom& g, int n_gr) {
     return pk;
 }
 
+// A unit's tail group (fused step only).  When every rank's shard ends in a
+// piece of at most 8 elements (S mod 4096 <= 8), those N_d pieces form one
+// tile instead of N_d: measured on GB300, each short tile otherwise cost
+// nearly a full tile's pass through the pipeline (P = 4M+13 at N_d = 64 ran
+// at 0.79 of the copy peak with its 64 one-element tiles and at 0.90 without
+// them).  Consumer thread r computes rank r's piece straight from global
+// memory: its gradients from every rank -- loaded KB ranks at a time, so that
+// the loads are in flight together -- summed in rank order with the same
+// two-sums, then the mean, AdamW, the bf16 cast and the gathered writes,
+// operation for operation as in the tiles (the scalar forms round exactly as
+// the packed ones), so the results are the same bits.
+template <int KB, int QMAX, class A>
+__device__ __forceinline__ void tail_group_sum(const A& a, const UnitDesc* u, int64_t e, int nv,
+                                               float (&sm)[8], float (&cm)[8]) {
+    // KB ranks x QMAX elements per batch, every load unconditional (indices
+    // clamped into the buffers; what is not needed is not summed), so that a
+    // batch's loads are in flight together
+    const int n = u->n_ranks;
+    for (int k0 = 0; k0 < n; k0 += KB) {
+        uint16_t x[KB][QMAX];
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk) {
+            const uint16_t* src = grad_ptr<uint16_t, A>(a, u, min(k0 + kk, n - 1)) + e;
+#pragma unroll
+            for (int q = 0; q < QMAX; ++q) x[kk][q] = src[min(q, nv - 1)];
+        }
+#pragma unroll
+        for (int kk = 0; kk < KB; ++kk) {
+            if (k0 + kk < n) {
+#pragma unroll
+                for (int q = 0; q < QMAX; ++q) {
+                    if (q < nv) two_sum_add1(sm[q], cm[q], bf16_to_float(x[kk][q]));
+                }
+            }
+        }
+    }
+}
+
+template <class A>
+__device__ __forceinline__ void tail_group_step(const A& a, const UnitDesc* u, int tid) {
+    const int64_t j0 = (u->S / kStagedTile) * kStagedTile;
+    const int r = tid;
+    if (r >= u->n_ranks) return;
+    const int64_t e = static_cast<int64_t>(r) * u->S + j0;
+    int64_t rem = u->S - j0;
+    if (u->P_valid - e < rem) rem = u->P_valid - e;
+    const int nv = static_cast<int>(rem > 0 ? (rem < kVec ? rem : kVec) : 0);
+    if (nv <= 0) return;
+    float sm[8], cm[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) sm[q] = cm[q] = 0.0f;
+    if (nv == 1) {
+        tail_group_sum<16, 1>(a, u, e, nv, sm, cm);
+    } else if (nv == 2) {
+        tail_group_sum<8, 2>(a, u, e, nv, sm, cm);
+    } else if (nv <= 4) {
+        tail_group_sum<4, 4>(a, u, e, nv, sm, cm);
+    } else {
+        tail_group_sum<2, 8>(a, u, e, nv, sm, cm);
+    }
+    float* master = ptr_at<float*, A>(a, u->off_master + r) + j0;
+    float* m = ptr_at<float*, A>(a, u->off_m + r) + j0;
+    float* v = ptr_at<float*, A>(a, u->off_v + r) + j0;
+    float th[8], mm[8], vv[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        const int qq = min(q, nv - 1);
+        th[q] = master[qq];
+        mm[q] = m[qq];
+        vv[q] = v[qq];
+    }
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+        if (q < nv) {
+            const float g = u->n_pow2 ? __fmul_rn(__fadd_rn(sm[q], cm[q]), u->inv_n)
+                                      : finish_mean(sm[q], cm[q], u->n_ranks_f, u->inv_n, false);
+            adamw_update(a.h.k, g, th[q], mm[q], vv[q]);
+            master[q] = th[q];
+            m[q] = mm[q];
+            v[q] = vv[q];
+            const uint16_t b = float_to_bf16_rn(th[q]);
+            for (int o = 0; o < u->n_out; ++o) ptr_at<uint16_t*, A>(a, u->off_out + o)[e + q] = b;
+        }
+    }
+}
+
 template <int MODE, class A, class GT, bool LEAD, bool PACK>
 __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                               volatile int* abort_flag, uint32_t* issued_out,
@@ -405,6 +509,23 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
     while (tile < total) {
         const TileGeom g = tile_geom<A, GT>(a, tile);
         if (g.nvalid == 0) {              // past the end of an unpadded parameter
+            tile = next_of(tile);
+            continue;
+        }
+        if (g.group) {
+            // A tail group reads nothing through the ring.  In the fixed order
+            // the consumers find it themselves; in the dynamic order an empty
+            // stage names it to them.
+            if (dyn) {
+                const uint32_t slot = it % kStages, parity = ((it / kStages) & 1) ^ 1;
+                if (!mbar_wait_bounded(smem_u32(&empty[slot]), parity, abort_flag, kWaitLimitNs)) {
+                    *issued_out = it;
+                    return;
+                }
+                tile_of[slot] = tile;
+                mbar_arrive(smem_u32(&full[slot]));
+                ++it;
+            }
             tile = next_of(tile);
             continue;
         }
@@ -483,6 +604,7 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
     constexpr int RG = GradTraits<GT>::kRanksPerStage;
     const bool dyn = a.h.sched_slot >= 0;
     int next_static = static_cast<int>(blockIdx.x);
+    uint64_t groups = 0;   // units (of at most 64 per launch) whose tail group this CTA took
     while (ok) {
         // The next tile: in the fixed order, or (dynamic scheduling) the one
         // the producer names in the tile's first stage, -1 when none is left.
@@ -610,6 +732,14 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
             ++it;
         };
 
+        if constexpr (MODE == kModePlain && sizeof(GT) == 2) {
+            if (g.group) {
+                // computed after the tile loop, whose registers are free then
+                groups |= 1ull << static_cast<int>(u - a.unit);
+                if (first_stage != nullptr) release();   // the empty stage that named it
+                continue;
+            }
+        }
         // The tile's first stage: its state arrays, then ranks [0, r0) (a
         // packed tile: all of them).
         const Packing pk = tile_packing<MODE, GT, LEAD, PACK>(g, n_gr);
@@ -780,6 +910,13 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                     }
                 }
             }
+        }
+    }
+    if constexpr (MODE == kModePlain && sizeof(GT) == 2) {
+        while (ok && groups != 0) {
+            const int ui = __ffsll(static_cast<long long>(groups)) - 1;
+            groups &= groups - 1;
+            tail_group_step<A>(a, &a.unit[ui], tid);
         }
     }
     if (lane == 0) atomicMin(consumed_min, it);
