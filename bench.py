@@ -591,15 +591,23 @@ def time_e2e_streamed(res, steps, warmup, ws, device):
     hp = dict(synthetic.ADAMW_DEFAULTS)
     fu0 = res.units[0]
     N, P_pad = fu0.n_ranks, fu0.P_pad
-    host_g = torch.empty((N, P_pad), dtype=torch.bfloat16, pin_memory=True)
-    for k in range(N):
+    # Distinct host gradient rows: all N_d when a quarter of the host's free
+    # memory, shared by the replicas on this host, holds them; else fewer,
+    # each standing in for several ranks.  Every rank's row still crosses the
+    # link every step, so the bytes moved do not change.
+    row_bytes = P_pad * 2
+    params_bytes = sum(fu.P_pad * 2 for fu in res.units)
+    budget = host_available_bytes() // 4 // max(ws, 1) - params_bytes
+    n_rows = int(max(1, min(N, budget // row_bytes)))
+    host_g = torch.empty((n_rows, P_pad), dtype=torch.bfloat16, pin_memory=True)
+    for k in range(n_rows):
         host_g[k].copy_(fu0.grads[k])
     host_p = [torch.empty(fu.P_pad, dtype=torch.bfloat16, pin_memory=True) for fu in res.units]
     spare = aligned_rows(N, P_pad, torch.bfloat16, device, 0)
     dev_sets = (fu0.grad_rows(), rows(spare))
     prepared = [[prepare_units([(g, *fu.state_rows(), None, fu.param_rows(), fu.layout)])
                  for g in dev_sets] for fu in res.units]
-    host_rows = [host_g[k] for k in range(N)]
+    host_rows = [host_g[k % n_rows] for k in range(N)]
     tables = [HostTables([host_rows], [hp_buf]) for hp_buf in host_p]
     h2d = len(res.units) * N * P_pad * 2
     d2h = sum(fu.P_pad * 2 for fu in res.units)
@@ -639,7 +647,23 @@ def time_e2e_streamed(res, steps, warmup, ws, device):
     barrier(ws)
     el = max_over_ranks(start.elapsed_time(stop) / 1e3, ws, device)
     del host_g, host_p, spare, prepared, tables, dev_sets
-    return el, h2d, d2h
+    return el, h2d, d2h, n_rows
+
+
+def host_available_bytes() -> int:
+    """Host memory available to this process now (MemAvailable), else the
+    physical memory, else a conservative 64 GB."""
+    try:
+        with open("/proc/meminfo") as f:
+            for line in f:
+                if line.startswith("MemAvailable:"):
+                    return int(line.split()[1]) * 1024
+    except OSError:
+        pass
+    try:
+        return os.sysconf("SC_PAGE_SIZE") * os.sysconf("SC_PHYS_PAGES")
+    except (ValueError, OSError, AttributeError):
+        return 64 << 30
 
 
 def _oracle_sample(E, workload="gpt2-small"):
@@ -1033,10 +1057,11 @@ def run_ours(args, ws, rank, local):
     if not args.no_e2e and args.variant == "plain" and w.n_micro == 1:
         if streamed:
             e2e_steps, e2e_warm = min(args.steps, 3), 1
-            e2e_el, h2d, d2h = time_e2e_streamed(res, e2e_steps, e2e_warm, ws, device)
+            e2e_el, h2d, d2h, n_rows = time_e2e_streamed(res, e2e_steps, e2e_warm, ws, device)
             how = ("every unit's gradient rows copied in and its parameters copied out each step, "
                    "unit by unit through two device gradient buffers; SM loads/stores through "
-                   "the pinned buffers' device mapping (ZERO_HOST_SM_COPY)")
+                   "the pinned buffers' device mapping (ZERO_HOST_SM_COPY); "
+                   f"{n_rows} distinct host gradient rows for the {w.n_ranks} ranks")
         else:
             e2e_steps, e2e_warm = args.steps, args.warmup
             e2e_el, h2d, d2h = time_e2e(res, e2e_steps, e2e_warm, ws, device)

@@ -66,6 +66,6 @@ def test_streamed_host_leg_byte_counts():
     res = bench.Resident(w, shared_grads=True)
     assert all(fu.grads is res.units[0].grads for fu in res.units)
     p_pad = synthetic.padded(100003, 8)
-    el, h2d, d2h = bench.time_e2e_streamed(res, 2, 1, 1, torch.device("cuda", 0))
-    assert el > 0
+    el, h2d, d2h, n_rows = bench.time_e2e_streamed(res, 2, 1, 1, torch.device("cuda", 0))
+    assert el > 0 and 1 <= n_rows <= 8
     assert h2d == 4 * 8 * p_pad * 2 and d2h == 4 * p_pad * 2

@@ -60,7 +60,10 @@ class ParamUnit:
         return all(bool(torch.all(b[-CANARY:] == SENTINEL)) for b in bufs)
 
 
-SHAPES = [(5, 3), (64, 7), (1, 11), (9, 1), (130, 2), (4096, 1), (33, 768), (1000, 13)]
+# At N_d = 8 the last two shapes have S = 4098 (S mod 4096 = 2: the fused step's tail group),
+# with the last rank's tail empty (32779 rows) or one element long (32783 rows).
+SHAPES = [(5, 3), (64, 7), (1, 11), (9, 1), (130, 2), (4096, 1), (33, 768), (1000, 13),
+          (32779, 1), (32783, 1)]
 
 
 @pytest.mark.parametrize("n_ranks", [3, 4, 8, 64])
