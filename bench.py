@@ -769,6 +769,7 @@ def run_reference(args, ws, rank, budget_s=90.0):
     that the whole run stays within about budget_s seconds."""
     if rank != 0:
         return 0
+    from fsdp_sharded_mixed_flatten_gb300 import synthetic
     threads = host_threads()
     cal = OracleRun(threads << 14, threads, args.workload)
     t0 = time.perf_counter()
@@ -799,8 +800,13 @@ def run_reference(args, ws, rank, budget_s=90.0):
             "ms_per_step": el / args.steps * 1e3, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "impl": "reference",
-            "config": {"workload": workload_label(args.workload), "sample": sample,
-                       "seed": args.seed},
+            "config": {"workload": workload_label(args.workload), "variant": args.variant,
+                       "seed": args.seed, "n_ranks_logical": run.w.n_ranks,
+                       "units": len(run.w.units), "params": sum(u.numel for u in run.w.units),
+                       "padded_elements": sum(synthetic.padded(u.numel, run.w.n_ranks)
+                                              for u in run.w.units),
+                       "storage": "bf16 grads/params, fp32 master/m/v", "n_out": 1,
+                       "sample": sample},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": threads, "kind": "oracle",
                              "cpu": cpu_model(), "sample": sample,
                              "extrapolated_full_step_s":
