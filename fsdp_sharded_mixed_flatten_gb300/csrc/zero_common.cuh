@@ -66,23 +66,52 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 // Knuth's error-free two-sum: after t = s + x, (s - (t - (t - s))) + (x - (t - s))
 // is exactly the rounding error of t.  The errors are collected in c, so that
 // s + c carries the running sum of the ranks' gradients to about twice fp32
-// precision.  Packed over element pairs with the sm_100+ FADD2/FFMA2 paths
-// (a - b is fma(b, -1, a): one rounding, the same as a subtraction).  The
-// scalar form below performs the identical IEEE operations lane by lane, so
-// the packed and scalar paths give bit-identical sums.
-
-__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
-    return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
-}
+// precision.  Packed over element pairs with the sm_100+ f32x2 additions
+// (FADD2), written in PTX on 64-bit register pairs from end to end: as C++ on
+// float2 values (a - b as an fma with a (-1, -1) pair) the compiler spent
+// about five register moves per two-sum forming pairs, and the clipped step's
+// norm pass, bound by instruction issue, ran 7 % more instructions and 1.4 %
+// slower.  The scalar form below performs the identical IEEE operations lane
+// by lane, so the packed and scalar paths give bit-identical sums.
 
 __device__ __forceinline__ void two_sum_add2(float2& s, float2& c, float2 x) {
-    const float2 t = __fadd2_rn(s, x);
-    const float2 bp = sub2(t, s);
-    const float2 ap = sub2(t, bp);
-    const float2 db = sub2(x, bp);
-    const float2 da = sub2(s, ap);
-    c = __fadd2_rn(c, __fadd2_rn(da, db));
-    s = t;
+    asm("{\n\t.reg .b64 xp, sp, cp, t, bp, ap, db, da, e;\n\t"
+        "mov.b64 xp, {%4, %5};\n\t"
+        "mov.b64 sp, {%0, %1};\n\t"
+        "mov.b64 cp, {%2, %3};\n\t"
+        "add.rn.f32x2 t, sp, xp;\n\t"
+        "sub.rn.f32x2 bp, t, sp;\n\t"
+        "sub.rn.f32x2 ap, t, bp;\n\t"
+        "sub.rn.f32x2 db, xp, bp;\n\t"
+        "sub.rn.f32x2 da, sp, ap;\n\t"
+        "add.rn.f32x2 e, da, db;\n\t"
+        "add.rn.f32x2 cp, cp, e;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t"
+        "mov.b64 {%2, %3}, cp;\n\t}"
+        : "+f"(s.x), "+f"(s.y), "+f"(c.x), "+f"(c.y)
+        : "f"(x.x), "f"(x.y));
+}
+
+// The same for two bf16 gradient values in one 32-bit word (lower index in the
+// low half), widened to fp32 inside the same PTX block.
+__device__ __forceinline__ void two_sum_add_bf16x2(float2& s, float2& c, uint32_t w) {
+    asm("{\n\t.reg .b32 xl, xh;\n\t.reg .b64 xp, sp, cp, t, bp, ap, db, da, e;\n\t"
+        "shl.b32 xl, %4, 16;\n\t"
+        "and.b32 xh, %4, 0xFFFF0000;\n\t"
+        "mov.b64 xp, {xl, xh};\n\t"
+        "mov.b64 sp, {%0, %1};\n\t"
+        "mov.b64 cp, {%2, %3};\n\t"
+        "add.rn.f32x2 t, sp, xp;\n\t"
+        "sub.rn.f32x2 bp, t, sp;\n\t"
+        "sub.rn.f32x2 ap, t, bp;\n\t"
+        "sub.rn.f32x2 db, xp, bp;\n\t"
+        "sub.rn.f32x2 da, sp, ap;\n\t"
+        "add.rn.f32x2 e, da, db;\n\t"
+        "add.rn.f32x2 cp, cp, e;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t"
+        "mov.b64 {%2, %3}, cp;\n\t}"
+        : "+f"(s.x), "+f"(s.y), "+f"(c.x), "+f"(c.y)
+        : "r"(w));
 }
 
 __device__ __forceinline__ float sub1(float a, float b) { return __fmaf_rn(b, -1.0f, a); }
@@ -111,10 +140,35 @@ __device__ __forceinline__ float finish_mean(float s, float c, float n_f, float 
 
 // Accumulate one rank's 8 bf16 gradient values (a 16-byte word group).
 __device__ __forceinline__ void two_sum_add_bf16x8(float2 (&s)[4], float2 (&c)[4], uint4 w) {
-    two_sum_add2(s[0], c[0], bf16x2_to_float2(w.x));
-    two_sum_add2(s[1], c[1], bf16x2_to_float2(w.y));
-    two_sum_add2(s[2], c[2], bf16x2_to_float2(w.z));
-    two_sum_add2(s[3], c[3], bf16x2_to_float2(w.w));
+    two_sum_add_bf16x2(s[0], c[0], w.x);
+    two_sum_add_bf16x2(s[1], c[1], w.y);
+    two_sum_add_bf16x2(s[2], c[2], w.z);
+    two_sum_add_bf16x2(s[3], c[3], w.w);
+}
+
+// The same two-sums written as C++ on float2 values (a - b as an fma with a
+// (-1, -1) pair): the same IEEE operations, so the same bits.  The direct-load
+// kernels use this form: they hold many loads in registers, and with the PTX
+// blocks ptxas spilled in them (up to 68 bytes).
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    return __ffma2_rn(b, make_float2(-1.0f, -1.0f), a);
+}
+
+__device__ __forceinline__ void two_sum_add2_c(float2& s, float2& c, float2 x) {
+    const float2 t = __fadd2_rn(s, x);
+    const float2 bp = sub2(t, s);
+    const float2 ap = sub2(t, bp);
+    const float2 db = sub2(x, bp);
+    const float2 da = sub2(s, ap);
+    c = __fadd2_rn(c, __fadd2_rn(da, db));
+    s = t;
+}
+
+__device__ __forceinline__ void two_sum_add_bf16x8_c(float2 (&s)[4], float2 (&c)[4], uint4 w) {
+    two_sum_add2_c(s[0], c[0], bf16x2_to_float2(w.x));
+    two_sum_add2_c(s[1], c[1], bf16x2_to_float2(w.y));
+    two_sum_add2_c(s[2], c[2], bf16x2_to_float2(w.z));
+    two_sum_add2_c(s[3], c[3], bf16x2_to_float2(w.w));
 }
 
 // ------------------------------------------------------------- loads -------

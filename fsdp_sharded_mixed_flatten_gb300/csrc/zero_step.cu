@@ -53,14 +53,14 @@ __device__ __forceinline__ void rank_sum_vec(const StepArgs<MAXR>& a, int64_t e0
             } else {
                 x = w0[u];
             }
-            two_sum_add_bf16x8(s, c, x);
+            two_sum_add_bf16x8_c(s, c, x);
         }
     }
     for (; k < n; ++k) {
         const uint16_t* p = a.grads[k] + ea;
         uint4 x = ld_stream(p);
         if constexpr (A != 0) x = align_shift<A>(x, ld_stream(p + 8));
-        two_sum_add_bf16x8(s, c, x);
+        two_sum_add_bf16x8_c(s, c, x);
     }
 }
 
