@@ -123,12 +123,13 @@ def test_7p5b_model_32_units_streamed_grads(oracle):
     _run(oracle, w, w.units, w.steps, 1, shared_grads=True, n_random=1000)
 
 
-def test_7p5b_units_fp32_accumulation_4_micro_steps(oracle):
-    """Full-size units of the 7.5B model with fp32 accumulation over 4
-    micro-steps (the accumulating form of the benchmark's 7.5B step), 4 units
-    sharing one gradient buffer, 2 optimizer steps."""
+def test_7p5b_model_fp32_accumulation_4_micro_steps(oracle):
+    """The whole 7.5B model with fp32 accumulation over 4 micro-steps, as the
+    benchmark runs it: 32 units sharing one gradient buffer, every micro-step
+    one zero_step_units call (two packed reduce-scatter launches for the first
+    three, four packed fused launches for the last), 2 optimizer steps."""
     w = synthetic.workload("7.5b-accum")
-    _run(oracle, w, w.units[:4], w.steps, 4, shared_grads=True)
+    _run(oracle, w, w.units, w.steps, 4, shared_grads=True, n_random=600)
 
 
 SWEEP = [(4 ** 10, 2), (4 ** 10 + 13, 64), (4 ** 12 + 13, 8), (4 ** 13, 64), (4 ** 14 + 13, 2),
