@@ -355,10 +355,8 @@ __device__ __forceinline__ void consume_stage_f32(const uint8_t* stage, int nk, 
         for (int kk = 0; kk < RMAX; ++kk) rank(kk);
         return;
     }
-#pragma unroll
-    for (int kk = 0; kk < RMAX; ++kk) {
-        if (kk < nk) rank(kk);
-    }
+#pragma unroll 1
+    for (int kk = 0; kk < nk; ++kk) rank(kk);
 }
 
 template <int A, int RMAX>
@@ -380,14 +378,18 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage, int nk, int 
         }
         return;
     }
-#pragma unroll
-    for (int kk = 0; kk < RMAX; ++kk) {
-        if (kk < nk) {
-            const uint4* p = reinterpret_cast<const uint4*>(base + kk * kSliceBytes);
-            uint4 x = p[0];
-            if constexpr (A != 0) x = align_shift<A>(x, p[1]);
-            two_sum_add_bf16x8(s, c, x);
-        }
+    // A partial stage (the last of a tile when N_d is not a multiple of 8):
+    // a rolled loop, so that the code of each misalignment stays small.  A
+    // short launch whose shards hold fewer tiles than the grid has CTAs
+    // that meet a different misalignment at every tile; with this path
+    // unrolled too they ran from a twice larger instruction footprint and
+    // measured 9 % slower (P = 4,194,317, N_d = 8).
+#pragma unroll 1
+    for (int kk = 0; kk < nk; ++kk) {
+        const uint4* p = reinterpret_cast<const uint4*>(base + kk * kSliceBytes);
+        uint4 x = p[0];
+        if constexpr (A != 0) x = align_shift<A>(x, p[1]);
+        two_sum_add_bf16x8(s, c, x);
     }
 }
 
@@ -1084,9 +1086,10 @@ static cudaError_t launch_as(const A& a, cudaStream_t stream) {
         reinterpret_cast<const void*>(&staged_step_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>);
     cudaError_t e = prepare_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>(kfn);
     if (e != cudaSuccess) return e;
-    // A norm launch runs exactly the CTAs whose partial-sum slots were
-    // counted (h.grid); the kernel has no inter-CTA dependence, so CTAs beyond
-    // the resident ones would only run in a later wave.
+    // h.grid when set: a norm launch runs exactly the CTAs whose partial-sum
+    // slots were counted, a short multi-stage launch its balanced grid (never
+    // more than the resident CTAs: the kernel has no inter-CTA dependence, and
+    // CTAs beyond the resident ones would only run in a later wave).
     const int grid = a.h.grid > 0 ? a.h.grid
                                   : persistent_grid(kfn, kTmaThreads, kStagedSmem, a.h.total_tiles);
     staged_step_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>
@@ -1143,6 +1146,18 @@ static cudaError_t launch_sized(MultiArgs& a, int n_ptrs, cudaStream_t stream) {
     if (!ModeTraits<MODE>::kNorm && a.h.grid == 0 &&
         a.h.total_tiles >= kDynamicMinRounds * grid_for<MODE, MultiArgsS>(a.h.total_tiles)) {
         a.h.sched_slot = sched_slot(stream);
+    }
+    // A short launch in the fixed order whose tiles span several stages (more
+    // than 8 ranks): as many CTAs as make every round full but the last, whose
+    // CTAs then finish together instead of a few of them running one more
+    // multi-stage tile while the rest idle.  Measured on GB300, P = 1,048,589
+    // and 4,194,304 at N_d = 64: 0.69 -> 0.71 and 0.92 -> 0.93 of the copy peak.
+    if (!ModeTraits<MODE>::kNorm && a.h.grid == 0 && a.h.sched_slot < 0 &&
+        ModeTraits<MODE>::kReadsGrads && !lead &&
+        max_ranks > GradTraits<GT>::kRanksPerStage) {
+        const int gmax = grid_for<MODE, MultiArgsS>(a.h.total_tiles);
+        const int rounds = (a.h.total_tiles + gmax - 1) / gmax;
+        a.h.grid = (a.h.total_tiles + rounds - 1) / rounds;
     }
     if constexpr (kHasAligned) {
         if (aligned) {
