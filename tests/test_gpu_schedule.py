@@ -1,11 +1,12 @@
-"""Dynamic tile order of the staged kernel.
+"""Tile order of the staged kernel.
 
-Launches whose tiles take one pass through the shared-memory ring (N_d <= 2,
-the clipped step's update pass) and that run many rounds of tiles let the CTAs
-claim tiles from a counter.  The results must not depend on the order: the
-same bits as the direct-load kernels (fixed order), eagerly, replayed from a
-CUDA graph, and on two streams at once.  Two launches forced onto one counter
-at the same time must never corrupt results silently: wrong bits come with
+Launches of at least 16 rounds of tiles (all but the norm passes) let the
+CTAs claim their tiles after the first from a counter; short launches whose
+tiles span several stages run in the fixed order on fewer CTAs than SMs.  The
+results must depend on neither the order nor the grid: the same bits as the
+direct-load kernels (fixed order, a CTA per SM), eagerly, replayed from a CUDA
+graph, and on two streams at once.  Two launches forced onto one counter at
+the same time must never corrupt results silently: wrong bits come with
 ZERO_DEVICE_SCHED_CONFLICT.
 """
 import pytest
@@ -58,24 +59,43 @@ def _step(u, t, stream=None):
                  stream=stream)
 
 
-def test_dynamic_order_equals_fixed_order(monkeypatch):
-    """The staged kernel (dynamic order here) against the direct-load kernels
-    (fixed order), 3 steps, bit for bit."""
+def _staged_equals_direct(monkeypatch, spec, tag):
+    """3 steps through the staged kernel and through the direct-load kernels
+    (fixed order, a CTA per SM), bit for bit."""
     runs = {}
     for kern in ("staged", "direct"):
         if kern == "direct":
             monkeypatch.setenv("ZERO_STEP_KERNEL", "direct")
         else:
             monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
-        u = _unit(BIG_N2, "dyn-vs-fixed")
+        u = _unit(spec, tag)
         for t in (1, 2, 3):
-            u.grads.copy_(_grads(u, t, "dyn-vs-fixed"))
+            u.grads.copy_(_grads(u, t, tag))
             _step(u, t)
         torch.cuda.synchronize()
         runs[kern] = _bits(u)
     monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
     assert _same(runs["staged"], runs["direct"])
     assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
+def test_dynamic_order_equals_fixed_order(monkeypatch):
+    """The staged kernel (dynamic order here) against the direct-load kernels."""
+    _staged_equals_direct(monkeypatch, BIG_N2, "dyn-vs-fixed")
+
+
+# Short launches in the fixed order whose tiles span several stages run on a
+# balanced grid (fewer CTAs than SMs, every round full but the last):
+#   N_d = 64, P = 1,048,589: S = 16,385 (S mod 8 = 1), 4 full tiles per rank
+#     plus the tail group = 257 tiles in 2 rounds of 129 CTAs (PACK form);
+#   N_d = 16, P = 1,600,048: S = 100,003, 400 tiles in 3 rounds of 134 CTAs;
+#   N_d = 32, P = 2,097,152: S = 65,536 (ALIGNED), 512 tiles in 4 rounds of 128.
+SHORT_MULTI_STAGE = [([1_000_000, 48_589], 64), ([1_600_000, 48], 16), ([2_097_152], 32)]
+
+
+@pytest.mark.parametrize("spec", SHORT_MULTI_STAGE, ids=["Nd64_pack", "Nd16", "Nd32_aligned"])
+def test_balanced_fixed_order_equals_direct(monkeypatch, spec):
+    _staged_equals_direct(monkeypatch, spec, f"balanced-{spec[1]}")
 
 
 def test_graph_replay_equals_eager():
