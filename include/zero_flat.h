@@ -35,7 +35,10 @@
  *     from a counter instead of taking them in a fixed order, so that faster
  *     SMs take more (the SMs' speeds differ by up to 40 % when a tile takes
  *     one pass through the kernel's shared-memory ring).  Results do not
- *     depend on the order.  Launches made directly use a counter per (device, stream);
+ *     depend on the order, nor on the grid: a shorter launch whose tiles
+ *     span several passes (more than 8 ranks) runs as many CTAs as make
+ *     every round of tiles full but the last.  Launches made directly use a
+ *     counter per (device, stream);
  *     launches captured into a CUDA graph take one of 1023 capture counters
  *     in turn.  Each launch leaves its counter at zero; if two launches ever
  *     claim from one counter at the same time (a stream destroyed while its
