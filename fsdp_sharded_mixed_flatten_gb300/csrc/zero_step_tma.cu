@@ -36,6 +36,7 @@
 #include <cstdlib>
 #include <limits>
 #include <mutex>
+#include <thread>
 #include <vector>
 #include <type_traits>
 
@@ -1189,7 +1190,9 @@ cudaError_t launch_staged_step_f32(MultiArgs& a, int n_ptrs, cudaStream_t stream
 // Scheduling slot of a launch on `stream` on the current device.  Launches
 // made directly get their stream's slot, one per (device, stream): a stream
 // runs its launches one after another and each launch leaves its slot at
-// zero, so launches sharing a slot never overlap.  Launches captured into a
+// zero, so launches sharing a slot never overlap.  The per-thread default
+// stream handle (cudaStreamPerThread) names a different stream in every host
+// thread, so it gets a slot per (device, thread).  Launches captured into a
 // CUDA graph take the capture slots in turn (a replay runs in whatever stream
 // the graph is launched into).  -1 (the fixed order) once the stream slots
 // are used up or when the stream's state cannot be read.  Two launches
@@ -1216,6 +1219,7 @@ int sched_slot(cudaStream_t stream) {
     struct Key {
         int dev;
         cudaStream_t stream;
+        std::thread::id thread;   // only for cudaStreamPerThread
         int slot;
     };
     static std::mutex mu;
@@ -1226,11 +1230,13 @@ int sched_slot(cudaStream_t stream) {
     if (cap != cudaStreamCaptureStatusNone) {
         return kStreamSlots + static_cast<int>(captured[dev]++ % (kSharedSlot - kStreamSlots));
     }
+    const std::thread::id thread =
+        stream == cudaStreamPerThread ? std::this_thread::get_id() : std::thread::id();
     for (const Key& k : keys) {
-        if (k.dev == dev && k.stream == stream) return k.slot;
+        if (k.dev == dev && k.stream == stream && k.thread == thread) return k.slot;
     }
     if (used[dev] >= kStreamSlots) return -1;
-    keys.push_back(Key{dev, stream, used[dev]++});
+    keys.push_back(Key{dev, stream, thread, used[dev]++});
     return keys.back().slot;
 }
 

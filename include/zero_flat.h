@@ -38,7 +38,8 @@
  *     depend on the order, nor on the grid: a shorter launch whose tiles
  *     span several passes (more than 8 ranks) runs as many CTAs as make
  *     every round of tiles full but the last.  Launches made directly use a
- *     counter per (device, stream);
+ *     counter per (device, stream), and per host thread on the per-thread
+ *     default stream (cudaStreamPerThread);
  *     launches captured into a CUDA graph take one of 1023 capture counters
  *     in turn.  Each launch leaves its counter at zero; if two launches ever
  *     claim from one counter at the same time (a stream destroyed while its

@@ -148,6 +148,48 @@ def test_two_streams_at_once_equal_one_after_the_other():
     assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
 
 
+def test_per_thread_default_stream_from_two_threads():
+    """The per-thread default stream handle (cudaStreamPerThread, 2) names a
+    different stream in every host thread.  Dynamically scheduled launches
+    from two threads on it at once use a counter each: no conflict is
+    recorded and the bits equal the same steps run one after the other."""
+    import threading
+    per_thread = 2
+    specs = [BIG_N2, ([12_000_001], 1)]
+    conc = [_unit(s, f"per-thread-{i}") for i, s in enumerate(specs)]
+    seq = [_unit(s, f"per-thread-{i}") for i, s in enumerate(specs)]
+    for i, (a, b) in enumerate(zip(conc, seq)):
+        g = _grads(a, 1, f"pt{i}")
+        a.grads.copy_(g)
+        b.grads.copy_(g)
+    torch.cuda.synchronize()
+    barrier = threading.Barrier(len(conc))
+    errors = []
+
+    def run(u):
+        try:
+            barrier.wait()
+            for t in (1, 2, 3):
+                _step(u, t, stream=per_thread)
+        except Exception as e:          # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=run, args=(u,)) for u in conc]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+    for u in seq:
+        for t in (1, 2, 3):
+            _step(u, t)
+    torch.cuda.synchronize()
+    for a, b in zip(conc, seq):
+        assert _same(_bits(a), _bits(b))
+
+
 def test_shared_counter_conflict_is_reported(monkeypatch):
     """Failure injection: with ZERO_SCHED_SHARED every dynamic launch claims
     from one counter, so launches on two streams at once may take tiles from
