@@ -394,36 +394,6 @@ __device__ __forceinline__ void consume_stage(const uint8_t* stage, int nk, int 
     }
 }
 
-// The PACK form (small launches with many ranks): a short tile that the
-// normal layout would spread over three or more stages (a rank's slice of a
-// few elements per 8 KB slot, 8 ranks a stage) travels as one packed stage
-// instead -- its state arrays and then every rank's slice, back to back, each
-// only as long as the tile needs.  A one-element tile at N_d = 64 then takes
-// one barrier round trip instead of nine, which matters when a launch has
-// only a few rounds of tiles.  The producer and the consumers decide from the
-// same geometry.  A separate template form, because the larger consumer loop
-// measured 0.5-1.2 % slower on launches that pack nothing.
-struct Packing {
-    int sstride;  // bytes from one state array to the next in the stage
-    int gstride;  // bytes from one rank's gradient slice to the next
-    bool on;
-};
-
-template <int MODE, class GT, bool LEAD, bool PACK>
-__device__ __forceinline__ Packing tile_packing(const TileGeom& g, int n_gr) {
-    constexpr int NS = ModeTraits<MODE>::kStateArrays;
-    constexpr int RG = GradTraits<GT>::kRanksPerStage;
-    Packing pk{kStateArrayBytes, slice_bytes<GT>(), false};
-    if constexpr (PACK && sizeof(GT) == 2 && ModeTraits<MODE>::kReadsGrads) {
-        if (g.nvalid < kStagedTile && n_gr > lead_ranks<NS, GT, LEAD>(n_gr) + RG) {
-            const int sst = g.state_valid * 4;                   // multiple of 16
-            const int gst = static_cast<int>(g.a1 - g.a0) * 2;   // multiple of 16
-            if (NS * sst + n_gr * gst <= kStageBytes) pk = Packing{sst, gst, true};
-        }
-    }
-    return pk;
-}
-
 // A unit's tail group (fused step only).  When every rank's shard ends in a
 // piece of at most 8 elements (S mod 4096 <= 8), those N_d pieces form one
 // tile instead of N_d: measured on GB300, each short tile otherwise cost
@@ -510,7 +480,7 @@ __device__ __forceinline__ void tail_group_step(const A& a, const UnitDesc* u, i
     }
 }
 
-template <int MODE, class A, class GT, bool LEAD, bool PACK>
+template <int MODE, class A, class GT, bool LEAD>
 __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_t* empty,
                               volatile int* abort_flag, uint32_t* issued_out,
                               volatile int* tile_of) {
@@ -557,10 +527,8 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
         const int n_ranks = ModeTraits<MODE>::kReadsGrads ? g.u->n_ranks : 0;
         const uint32_t sbytes = static_cast<uint32_t>(g.state_valid) * 4;
         const uint32_t gbytes = static_cast<uint32_t>(g.a1 - g.a0) * sizeof(GT);
-        // stage 0: state arrays + ranks [0, r0); then RG ranks per stage (a
-        // packed tile: everything in stage 0)
-        const Packing pk = tile_packing<MODE, GT, LEAD, PACK>(g, n_ranks);
-        const int r0 = pk.on ? n_ranks : lead_ranks<NS, GT, LEAD>(n_ranks);
+        // stage 0: state arrays + ranks [0, r0); then RG ranks per stage
+        const int r0 = lead_ranks<NS, GT, LEAD>(n_ranks);
         const int n_stages = 1 + (n_ranks - r0 + RG - 1) / RG;
         bool stop = false;
         for (int st = 0; st < n_stages; ++st) {
@@ -580,14 +548,14 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
             const uint32_t dst = smem_u32(smem + slot * kStageBytes);
             if (sbytes > 0) {
                 for (int arr = 0; arr < ns; ++arr) {
-                    bulk_copy_g2s(dst + arr * pk.sstride,
+                    bulk_copy_g2s(dst + arr * kStateArrayBytes,
                                   state_ptr<MODE, A>(a, g.u, arr, g.r) + g.j0, sbytes, bar);
                 }
             }
             if (gbytes > 0) {
-                const uint32_t gdst = dst + ns * pk.sstride;
+                const uint32_t gdst = dst + ns * kStateArrayBytes;
                 for (int kk = 0; kk < nk; ++kk) {
-                    bulk_copy_g2s(gdst + kk * pk.gstride, grad_ptr<GT, A>(a, g.u, k0 + kk) + g.a0,
+                    bulk_copy_g2s(gdst + kk * slice_bytes<GT>(), grad_ptr<GT, A>(a, g.u, k0 + kk) + g.a0,
                                   gbytes, bar);
                 }
             }
@@ -612,7 +580,7 @@ __device__ void producer_loop(const A& a, uint8_t* smem, uint64_t* full, uint64_
     *issued_out = it;
 }
 
-template <int MODE, class A, class GT, bool LEAD, bool ALIGNED, bool PACK>
+template <int MODE, class A, class GT, bool LEAD, bool ALIGNED>
 __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                               uint64_t* empty, volatile int* abort_flag,
                               unsigned int* consumed_min, float clip_coef, double* warp_sq,
@@ -714,33 +682,6 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                 }
             }
         };
-        // Every rank from one packed stage (PACK form), element by element:
-        // the same two-sums as the packed-pair path, lane by lane.  A packed
-        // tile is short, so this path stays small instead of fast.  An
-        // element past the last full 16 bytes of a buffer is not in the stage
-        // and comes from global memory.
-        auto consume_packed = [&](const uint8_t* stage, int nk, int stride) {
-            if constexpr (PACK && sizeof(GT) == 2) {
-                if (nv > 0) {
-                    for (int kk = 0; kk < nk; ++kk) {
-                        const GT* src = grad_ptr<GT, A>(a, u, kk) + e;
-                        const GT* sm =
-                            reinterpret_cast<const GT*>(stage + kk * stride) + (first + g.mis);
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            if (2 * q < nv) {
-                                const GT x = e + 2 * q < g.a1 ? sm[2 * q] : src[2 * q];
-                                two_sum_add1(s[q].x, c[q].x, GradTraits<GT>::widen(x));
-                            }
-                            if (2 * q + 1 < nv) {
-                                const GT x = e + 2 * q + 1 < g.a1 ? sm[2 * q + 1] : src[2 * q + 1];
-                                two_sum_add1(s[q].y, c[q].y, GradTraits<GT>::widen(x));
-                            }
-                        }
-                    }
-                }
-            }
-        };
         // Wait for the ring's next stage; the outcome is made warp-uniform so
         // that the warp's later shuffles see every lane.
         auto wait_full = [&]() -> const uint8_t* {
@@ -765,10 +706,8 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                 continue;
             }
         }
-        // The tile's first stage: its state arrays, then ranks [0, r0) (a
-        // packed tile: all of them).
-        const Packing pk = tile_packing<MODE, GT, LEAD, PACK>(g, n_gr);
-        const int r0 = pk.on ? n_gr : lead_ranks<NS, GT, LEAD>(n_gr);
+        // The tile's first stage: its state arrays, then ranks [0, r0).
+        const int r0 = lead_ranks<NS, GT, LEAD>(n_gr);
         {
             const uint8_t* stage = first_stage != nullptr ? first_stage : wait_full();
             if (stage == nullptr) {
@@ -782,7 +721,7 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                     // every 8 read their upper word first, so that each
                     // quarter-warp's 16-byte reads fall in distinct banks.
                     const float4* p =
-                        reinterpret_cast<const float4*>(stage + arr * pk.sstride + first * 4);
+                        reinterpret_cast<const float4*>(stage + arr * kStateArrayBytes + first * 4);
                     const int sw = (tid >> 2) & 1;
                     const float4 ya = p[sw], yb = p[sw ^ 1];
                     const float4 x0 = sw ? yb : ya, x1 = sw ? ya : yb;
@@ -794,20 +733,16 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
                     for (int t = 0; t < kVec; ++t) st[arr][t] = (t < nv) ? src[t] : 0.0f;
                 }
             }
-            if (pk.on) {
-                consume_packed(stage + NS * pk.sstride, n_gr, pk.gstride);
-            } else {
-                if constexpr (NS == 0 || LEAD) {
-                    constexpr int kFirstMax = NS == 0 ? RG : first_stage_ranks<GT>(NS);
-                    if (r0 > 0) {
-                        consume(stage + NS * kStateArrayBytes, 0, r0,
-                                std::integral_constant<int, kFirstMax>());
-                    }
+            if constexpr (NS == 0 || LEAD) {
+                constexpr int kFirstMax = NS == 0 ? RG : first_stage_ranks<GT>(NS);
+                if (r0 > 0) {
+                    consume(stage + NS * kStateArrayBytes, 0, r0,
+                            std::integral_constant<int, kFirstMax>());
                 }
             }
             release();
         }
-        // Then RG ranks per stage (none left in a LEAD launch or a packed tile).
+        // Then RG ranks per stage (none left in a LEAD launch).
         if constexpr (NS == 0 || !LEAD) {
             for (int k0 = r0; k0 < n_gr; k0 += RG) {
                 const uint8_t* stage = wait_full();
@@ -962,8 +897,7 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
 // every unit's shard length S is a multiple of 8, so every rank's slice and
 // every thread's 8 elements start on the 16-byte grid and no realignment code
 // is compiled in.
-template <int MODE, class A, class GT = uint16_t, bool LEAD = false, bool ALIGNED = false,
-          bool PACK = false>
+template <int MODE, class A, class GT = uint16_t, bool LEAD = false, bool ALIGNED = false>
 __global__ void __launch_bounds__(kTmaThreads, 1)
 staged_step_kernel(const __grid_constant__ A a) {
     extern __shared__ __align__(128) uint8_t smem[];
@@ -1012,11 +946,11 @@ staged_step_kernel(const __grid_constant__ A a) {
     __syncthreads();
     if (threadIdx.x >= kConsumers) {
         if (threadIdx.x == kConsumers) {
-            producer_loop<MODE, A, GT, LEAD, PACK>(a, smem, full, empty, &abort_flag, &issued,
+            producer_loop<MODE, A, GT, LEAD>(a, smem, full, empty, &abort_flag, &issued,
                                                    tile_of);
         }
     } else {
-        consumer_loop<MODE, A, GT, LEAD, ALIGNED, PACK>(a, smem, full, empty, &abort_flag,
+        consumer_loop<MODE, A, GT, LEAD, ALIGNED>(a, smem, full, empty, &abort_flag,
                                                         &consumed_min, clip_coef, warp_sq,
                                                         tile_of);
     }
@@ -1059,8 +993,7 @@ staged_step_kernel(const __grid_constant__ A a) {
 constexpr size_t kStagedSmem = static_cast<size_t>(kStages) * kStageBytes;
 
 // Raise the kernel's dynamic shared-memory limit once per device.
-template <int MODE, class A, class GT = uint16_t, bool LEAD = false, bool ALIGNED = false,
-          bool PACK = false>
+template <int MODE, class A, class GT = uint16_t, bool LEAD = false, bool ALIGNED = false>
 static cudaError_t prepare_kernel(const void* kfn) {
     static std::atomic<uint64_t> done_mask{0};
     int dev = 0;
@@ -1081,11 +1014,11 @@ static int grid_for(int total_tiles) {
     return persistent_grid(kfn, kTmaThreads, kStagedSmem, total_tiles);
 }
 
-template <int MODE, class A, class GT, bool LEAD, bool ALIGNED, bool PACK>
+template <int MODE, class A, class GT, bool LEAD, bool ALIGNED>
 static cudaError_t launch_as(const A& a, cudaStream_t stream) {
     const void* kfn =
-        reinterpret_cast<const void*>(&staged_step_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>);
-    cudaError_t e = prepare_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>(kfn);
+        reinterpret_cast<const void*>(&staged_step_kernel<MODE, A, GT, LEAD, ALIGNED>);
+    cudaError_t e = prepare_kernel<MODE, A, GT, LEAD, ALIGNED>(kfn);
     if (e != cudaSuccess) return e;
     // h.grid when set: a norm launch runs exactly the CTAs whose partial-sum
     // slots were counted, a short multi-stage launch its balanced grid (never
@@ -1093,7 +1026,7 @@ static cudaError_t launch_as(const A& a, cudaStream_t stream) {
     // CTAs beyond the resident ones would only run in a later wave).
     const int grid = a.h.grid > 0 ? a.h.grid
                                   : persistent_grid(kfn, kTmaThreads, kStagedSmem, a.h.total_tiles);
-    staged_step_kernel<MODE, A, GT, LEAD, ALIGNED, PACK>
+    staged_step_kernel<MODE, A, GT, LEAD, ALIGNED>
         <<<grid, kTmaThreads, kStagedSmem, stream>>>(a);
     return cudaGetLastError();
 }
@@ -1110,13 +1043,13 @@ static const A& shrink(const MultiArgs& big, int n_ptrs) {
 
 // The smaller argument block when the launch fits it (a launch copies its
 // whole block), else the full one.
-template <int MODE, class GT, bool LEAD, bool ALIGNED, bool PACK = false>
+template <int MODE, class GT, bool LEAD, bool ALIGNED>
 static cudaError_t launch_form(const MultiArgs& a, int n_ptrs, cudaStream_t stream) {
     if (a.h.n_units <= MultiArgsS::kUnits && n_ptrs <= MultiArgsS::kPtrs) {
-        return launch_as<MODE, MultiArgsS, GT, LEAD, ALIGNED, PACK>(
+        return launch_as<MODE, MultiArgsS, GT, LEAD, ALIGNED>(
             shrink<MultiArgsS>(a, n_ptrs), stream);
     }
-    return launch_as<MODE, MultiArgs, GT, LEAD, ALIGNED, PACK>(a, stream);
+    return launch_as<MODE, MultiArgs, GT, LEAD, ALIGNED>(a, stream);
 }
 
 // Pick the kernel form: LEAD when every unit's whole tile fits one stage, the
@@ -1170,14 +1103,6 @@ static cudaError_t launch_sized(MultiArgs& a, int n_ptrs, cudaStream_t stream) {
     }
     if constexpr (kCanLead) {
         if (lead) return launch_form<MODE, GT, true, false>(a, n_ptrs, stream);
-    }
-    if constexpr (MODE == kModePlain && sizeof(GT) == 2) {
-        // PACK: more than 16 ranks (a tail tile spans three or more stages)
-        // and fewer than 16 rounds of tiles, where the tails' pipeline passes
-        // are a visible part of the launch
-        if (max_ranks > 16 && a.h.total_tiles < 16 * grid_for<MODE, MultiArgsS>(a.h.total_tiles)) {
-            return launch_form<MODE, GT, false, false, true>(a, n_ptrs, stream);
-        }
     }
     return launch_form<MODE, GT, false, false>(a, n_ptrs, stream);
 }

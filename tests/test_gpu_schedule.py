@@ -87,13 +87,17 @@ def test_dynamic_order_equals_fixed_order(monkeypatch):
 # Short launches in the fixed order whose tiles span several stages run on a
 # balanced grid (fewer CTAs than SMs, every round full but the last):
 #   N_d = 64, P = 1,048,589: S = 16,385 (S mod 8 = 1), 4 full tiles per rank
-#     plus the tail group = 257 tiles in 2 rounds of 129 CTAs (PACK form);
+#     plus the tail group = 257 tiles in 2 rounds of 129 CTAs;
 #   N_d = 16, P = 1,600,048: S = 100,003, 400 tiles in 3 rounds of 134 CTAs;
-#   N_d = 32, P = 2,097,152: S = 65,536 (ALIGNED), 512 tiles in 4 rounds of 128.
-SHORT_MULTI_STAGE = [([1_000_000, 48_589], 64), ([1_600_000, 48], 16), ([2_097_152], 32)]
+#   N_d = 32, P = 2,097,152: S = 65,536 (ALIGNED), 512 tiles in 4 rounds of 128;
+#   N_d = 32, P = 1,051,776: S = 32,868 (S mod 8 = 4), 8 full tiles per rank
+#     and a 100-element tail tile each = 288 tiles in 2 rounds of 144 CTAs.
+SHORT_MULTI_STAGE = [([1_000_000, 48_589], 64), ([1_600_000, 48], 16), ([2_097_152], 32),
+                     ([1_051_776], 32)]
 
 
-@pytest.mark.parametrize("spec", SHORT_MULTI_STAGE, ids=["Nd64_pack", "Nd16", "Nd32_aligned"])
+@pytest.mark.parametrize("spec", SHORT_MULTI_STAGE,
+                         ids=["Nd64_tail_group", "Nd16", "Nd32_aligned", "Nd32_tail100"])
 def test_balanced_fixed_order_equals_direct(monkeypatch, spec):
     _staged_equals_direct(monkeypatch, spec, f"balanced-{spec[1]}")
 
