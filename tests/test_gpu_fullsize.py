@@ -133,7 +133,10 @@ def test_7p5b_model_fp32_accumulation_4_micro_steps(oracle):
 
 
 SWEEP = [(4 ** 10, 2), (4 ** 10 + 13, 64), (4 ** 12 + 13, 8), (4 ** 13, 64), (4 ** 14 + 13, 2),
-         (4 ** 15 + 13, 64), (4 ** 15, 8)]
+         (4 ** 15 + 13, 64), (4 ** 15, 8),
+         # S = 65,822: every rank's shard ends in 286 elements, as the 7.5B
+         # model's do, in a launch of 7 rounds
+         (64 * 65822, 64)]
 
 
 @pytest.mark.parametrize("P,n_ranks", SWEEP, ids=[f"P{p}_N{n}" for p, n in SWEEP])

@@ -56,6 +56,13 @@ CASES = [
     ("aligned_one_rank_two_outputs", [8 * 1111, 8 * 7], 1, 2, 1, 2),
     ("aligned_eight_ranks_two_outputs", [8 * 8 * 3001], 8, 2, 1, 2),
     ("aligned_accumulate_3_micro_steps", [16 * 8 * 777], 16, 1, 3, 2),
+    # shards ending in a tail of 13..509 elements at N_d > 8: one short tile
+    # per rank spanning several stages (S = 4196: 100-element tails, the last
+    # rank's ending past the buffer's last full 16 bytes; S = 8701: S mod 8 = 5;
+    # S = 4109 with N_d = 9)
+    ("ranks_64_tail_100_two_group_tiles", [64 * 4196 - 3], 64, 1, 1, 2),
+    ("ranks_16_tail_509", [16 * 8701], 16, 1, 1, 2),
+    ("ranks_9_tail_13", [9 * 4109 - 4], 9, 2, 1, 2),
 ]
 
 
@@ -86,7 +93,9 @@ def test_small_cases(oracle, kernel, name, numels, n_ranks, n_out, n_micro, step
                                                     ([999999], 3, 1), ([64 * 4099 + 5], 64, 2),
                                                     ([77777], 65, 3), ([5], 8, 1),
                                                     ([2 * 8 * 70001], 2, 1),
-                                                    ([8 * 8 * 1234], 8, 2)])
+                                                    ([8 * 8 * 1234], 8, 2),
+                                                    ([64 * 4196 - 3], 64, 1),
+                                                    ([16 * 8701], 16, 1)])
 def test_staged_equals_direct_bitwise(monkeypatch, numels, n_ranks, n_micro):
     """The bulk-copy staged kernels and the direct-load kernels give identical bits."""
     units = {}
@@ -271,7 +280,13 @@ def _unit_tuple(u, accum):
     [([1000 + 37 * i], 1 + (i % 9)) for i in range(80)],
     # pointer-limited packing: 64 ranks per unit -> at most 13 units per launch
     [([64 * 53 + i], 64) for i in range(20)],
-], ids=["gpt2_like", "80_units_mixed", "pointer_limited"])
+    # 512-element tails at N_d = 64, 12 units in one launch
+    [([64 * 4608 - i], 64) for i in range(12)],
+    # tails of 9..453 elements at assorted N_d > 8
+    [([n * (4096 + 9 + 37 * i) - i % 3], n)
+     for i, n in enumerate([9, 16, 33, 64, 64, 100, 12, 64, 17, 64, 128, 64, 64])],
+], ids=["gpt2_like", "80_units_mixed", "pointer_limited", "long_tails_64_ranks",
+        "long_tails_mixed"])
 def test_step_units_equals_per_unit_steps(kernel, specs, n_micro):
     """zero_step_units over many FlatParameters is bit-identical to one
     zero_step per unit."""
