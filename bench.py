@@ -765,8 +765,11 @@ def cpu_baseline(workload="7.5b", seconds=8.0):
 
 def run_reference(args, ws, rank, budget_s=90.0):
     """The oracle as the reference arm: W untimed and K timed steps, each over
-    a contiguous sample of the workload sized (from a short calibration) so
-    that the whole run stays within about budget_s seconds."""
+    a contiguous sample of the workload sized from a short calibration so that
+    the whole run takes at most about budget_s seconds.  The sample is also
+    capped at 2^21 flat elements and 2^25 gradient values per thread, which
+    bound its host memory (at N_d = 64 the second cap binds: 2^19 elements
+    per thread)."""
     if rank != 0:
         return 0
     from fsdp_sharded_mixed_flatten_gb300 import synthetic
