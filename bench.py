@@ -732,33 +732,44 @@ class OracleRun:
         self.pool.shutdown()
 
 
+def _timed_oracle_steps(run, seconds):
+    """Step an OracleRun until `seconds` have passed; (steps, elapsed s)."""
+    reps = 0
+    t0 = time.perf_counter()
+    while True:
+        reps += 1
+        run.step(reps)
+        el = time.perf_counter() - t0
+        if el >= seconds:
+            return reps, el
+
+
 def cpu_baseline(workload="7.5b", seconds=8.0):
     """The CPU oracle as it stands, on a bounded contiguous sample of the
     workload (all N_d ranks): one chunk per host core of 2^23 / N_d flat
     elements (so that a chunk holds 2^23 gradient values whatever N_d is), the
-    chunks stepped in parallel for about `seconds`."""
+    chunks stepped in parallel for about `seconds`; then one such chunk on a
+    single thread for a quarter of that (the single-core rate)."""
     from fsdp_sharded_mixed_flatten_gb300 import synthetic
     threads = host_threads()
     n_ranks = synthetic.workload(workload).n_ranks
     per = max(1 << 12, (1 << 23) // n_ranks) & ~7
     run = OracleRun(threads * per, threads, workload)
-    reps, step = 0, 0
-    t0 = time.perf_counter()
-    while True:
-        step += 1
-        run.step(step)
-        reps += 1
-        el = time.perf_counter() - t0
-        if el >= seconds:
-            break
+    reps, el = _timed_oracle_steps(run, seconds)
     run.close()
     rate = reps * run.E / el
+    one = OracleRun(per, 1, workload)
+    reps1, el1 = _timed_oracle_steps(one, seconds / 4)
+    one.close()
+    rate1 = reps1 * one.E / el1
     return {"value": rate, "unit": UNIT, "cores": threads, "kind": "oracle",
             "cpu": cpu_model(),
             "extrapolated_full_step_s": sum(u.numel for u in run.w.units) / rate,
+            "single_thread_value": rate1,
             "sample": f"{run.E} contiguous flat elements x {run.w.n_ranks} ranks of the {workload} "
                       f"workload in {len(run.chunks)} chunks, one per thread; {reps} oracle steps "
-                      f"in {el:.1f} s (double arithmetic)"}
+                      f"in {el:.1f} s (double arithmetic); single thread: {one.E} elements, "
+                      f"{reps1} steps in {el1:.1f} s"}
 
 
 # ----------------------------------------------------------------- arms ----
