@@ -138,6 +138,44 @@ __device__ __forceinline__ float finish_mean(float s, float c, float n_f, float 
     return __fadd_rn(q, __fdiv_rn(__fadd_rn(r, c), n_f));
 }
 
+// The first rank's values start the sum: s = x + 0 and c = s - s are exactly
+// what a two-sum of x into (0, 0) leaves (+0 for a -0 input, +0 error terms
+// for finite values, NaN error terms for infinities and NaNs), in two packed
+// additions instead of seven.
+__device__ __forceinline__ void first_rank2(float2& s, float2& c, float2 x) {
+    asm("{\n\t.reg .b64 xp, zp, t, e;\n\t"
+        "mov.b64 xp, {%4, %5};\n\t"
+        "mov.b64 zp, 0;\n\t"
+        "add.rn.f32x2 t, zp, xp;\n\t"
+        "sub.rn.f32x2 e, t, t;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t"
+        "mov.b64 {%2, %3}, e;\n\t}"
+        : "=f"(s.x), "=f"(s.y), "=f"(c.x), "=f"(c.y)
+        : "f"(x.x), "f"(x.y));
+}
+
+// The same for two bf16 values in one word, widened inside the PTX block.
+__device__ __forceinline__ void first_rank_bf16x2(float2& s, float2& c, uint32_t w) {
+    asm("{\n\t.reg .b32 xl, xh;\n\t.reg .b64 xp, zp, t, e;\n\t"
+        "shl.b32 xl, %4, 16;\n\t"
+        "and.b32 xh, %4, 0xFFFF0000;\n\t"
+        "mov.b64 xp, {xl, xh};\n\t"
+        "mov.b64 zp, 0;\n\t"
+        "add.rn.f32x2 t, zp, xp;\n\t"
+        "sub.rn.f32x2 e, t, t;\n\t"
+        "mov.b64 {%0, %1}, t;\n\t"
+        "mov.b64 {%2, %3}, e;\n\t}"
+        : "=f"(s.x), "=f"(s.y), "=f"(c.x), "=f"(c.y)
+        : "r"(w));
+}
+
+__device__ __forceinline__ void first_rank_bf16x8(float2 (&s)[4], float2 (&c)[4], uint4 w) {
+    first_rank_bf16x2(s[0], c[0], w.x);
+    first_rank_bf16x2(s[1], c[1], w.y);
+    first_rank_bf16x2(s[2], c[2], w.z);
+    first_rank_bf16x2(s[3], c[3], w.w);
+}
+
 // Accumulate one rank's 8 bf16 gradient values (a 16-byte word group).
 __device__ __forceinline__ void two_sum_add_bf16x8(float2 (&s)[4], float2 (&c)[4], uint4 w) {
     two_sum_add_bf16x2(s[0], c[0], w.x);

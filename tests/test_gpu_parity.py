@@ -311,6 +311,52 @@ def test_step_units_equals_per_unit_steps(kernel, specs, n_micro):
                            b.params.contiguous().view(torch.int16))
 
 
+# bf16 bit patterns: -0, +inf, -inf, NaN, the smallest subnormals of both signs
+SPECIAL_BF16 = [0x8000, 0x7F80, 0xFF80, 0x7FC0, 0x0001, 0x8001]
+
+
+@pytest.mark.parametrize("n_ranks", [1, 2, 3, 8, 64])
+def test_special_values_staged_equals_direct(monkeypatch, n_ranks):
+    """Signed zeros, infinities, NaNs and subnormals, in rank 0 (whose values
+    start the staged kernel's sums without a two-sum) and in later ranks, give
+    the same bits through the staged kernel and the direct-load kernels, whose
+    sums start from (0, 0)."""
+    P = n_ranks * (2 * 4096 + 77) + 3
+    g = synthetic.make_grads(P, n_ranks, 1e-2, ("special", n_ranks))
+    gi = g.view(torch.int16)
+    P_pad = g.shape[1]
+    rng = np.random.default_rng(n_ranks)
+    for k in sorted({0, n_ranks - 1, n_ranks // 2}):
+        pos = rng.choice(P_pad, size=96, replace=False)
+        vals = np.array(SPECIAL_BF16 * 16, dtype=np.uint16).view(np.int16)
+        gi[k, torch.from_numpy(pos)] = torch.from_numpy(vals)
+    # every rank -0 at a few elements (the sum's sign of zero)
+    gi[:, :64] = torch.tensor(np.uint16(0x8000).view(np.int16))
+    master0 = synthetic.make_master_flat(P, n_ranks, 0.02, ("special-m", n_ranks))
+    master0[:32] = -0.0
+    runs = {}
+    for kern in ("staged", "direct"):
+        if kern == "direct":
+            monkeypatch.setenv("ZERO_STEP_KERNEL", "direct")
+        else:
+            monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
+        u = FlatUnit([P], n_ranks, n_out=1)
+        u.set_master_flat(master0.cuda())
+        u.grads.copy_(g.cuda())
+        for t in (1, 2):
+            zf.zero_step(u.grad_rows(), *u.state_rows(), None, 1, 1, u.param_rows(), u.layout,
+                         hp_at(t))
+        rs = aligned_rows(n_ranks, u.S, torch.float32, "cuda", 0)
+        zf.zero_reduce_scatter(u.grad_rows(), rows(rs), u.layout, 0)
+        torch.cuda.synchronize()
+        runs[kern] = [x.contiguous().view(torch.int32).clone() for x in (u.master, u.m, u.v, rs)] + \
+            [u.params.contiguous().view(torch.int16).clone()]
+    monkeypatch.delenv("ZERO_STEP_KERNEL", raising=False)
+    for x, y in zip(runs["staged"], runs["direct"]):
+        assert torch.equal(x, y)
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
+
 def test_step_units_against_oracle(oracle):
     """Three units of different shapes stepped together, each checked against
     the oracle."""
