@@ -610,9 +610,12 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
     const int lane = tid & 31;
     uint32_t it = 0;
     bool ok = true;
-    // compensated sums of squares (norm modes): packed pairs for whole groups,
-    // a scalar pair for the ragged end
+    // compensated sums of squares (norm modes): two packed accumulators for
+    // whole groups (element pairs 0, 2 and 1, 3: half the dependency chain of
+    // one, measured +0.35 % on the clipped GPT-2-small step), a scalar pair
+    // for the ragged end
     float2 sq2_s = make_float2(0.0f, 0.0f), sq2_c = make_float2(0.0f, 0.0f);
+    float2 sq3_s = make_float2(0.0f, 0.0f), sq3_c = make_float2(0.0f, 0.0f);
     float sq_s = 0.0f, sq_c = 0.0f;
     constexpr int RG = GradTraits<GT>::kRanksPerStage;
     const bool dyn = a.h.sched_slot >= 0;
@@ -810,7 +813,11 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         const float2 o = make_float2(out[2 * q], out[2 * q + 1]);
-                        two_sum_add2(sq2_s, sq2_c, __fmul2_rn(o, o));
+                        if (q & 1) {
+                            two_sum_add2(sq3_s, sq3_c, __fmul2_rn(o, o));
+                        } else {
+                            two_sum_add2(sq2_s, sq2_c, __fmul2_rn(o, o));
+                        }
                     }
                 } else {
 #pragma unroll
@@ -902,7 +909,9 @@ __device__ void consumer_loop(const A& a, const uint8_t* smem, uint64_t* full,
     if (lane == 0) atomicMin(consumed_min, it);
     if constexpr (ModeTraits<MODE>::kNorm) {
         // Warp sum of the threads' compensated sums, in double, fixed order.
-        double w = static_cast<double>(sq2_s.x) + static_cast<double>(sq2_c.x) +
+        double w = static_cast<double>(sq3_s.x) + static_cast<double>(sq3_c.x) +
+                   static_cast<double>(sq3_s.y) + static_cast<double>(sq3_c.y) +
+                   static_cast<double>(sq2_s.x) + static_cast<double>(sq2_c.x) +
                    static_cast<double>(sq2_s.y) + static_cast<double>(sq2_c.y) +
                    static_cast<double>(sq_s) + static_cast<double>(sq_c);
 #pragma unroll
