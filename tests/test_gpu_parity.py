@@ -324,10 +324,9 @@ def test_special_values_staged_equals_direct(monkeypatch, n_ranks):
     P = n_ranks * (2 * 4096 + 77) + 3
     g = synthetic.make_grads(P, n_ranks, 1e-2, ("special", n_ranks))
     gi = g.view(torch.int16)
-    P_pad = g.shape[1]
     rng = np.random.default_rng(n_ranks)
     for k in sorted({0, n_ranks - 1, n_ranks // 2}):
-        pos = rng.choice(P_pad, size=96, replace=False)
+        pos = rng.choice(P, size=96, replace=False)     # the padding stays zero
         vals = np.array(SPECIAL_BF16 * 16, dtype=np.uint16).view(np.int16)
         gi[k, torch.from_numpy(pos)] = torch.from_numpy(vals)
     # every rank -0 at a few elements (the sum's sign of zero)

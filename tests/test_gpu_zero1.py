@@ -94,3 +94,43 @@ def test_zero1_equals_zero2_on_exact_inputs():
         assert torch.equal(x.contiguous().view(torch.int32), y.contiguous().view(torch.int32))
     assert torch.equal(a.params.contiguous().view(torch.int16),
                        b.params.contiguous().view(torch.int16))
+
+
+@pytest.mark.parametrize("n_ranks", [1, 3, 8, 64])
+def test_zero1_equals_plain_step_on_special_values(n_ranks):
+    """With one micro-step the ZeRO-1 form sums the same values as the plain
+    step (its fp32 accumulators are the exactly widened bf16 gradients) in the
+    same rank order, so the two give identical bits: signed zeros,
+    infinities, NaNs and subnormals included, in rank 0 (whose values start
+    both sums without a two-sum) and in later ranks."""
+    numels = [n_ranks * (2 * 4096 + 77) + 3]
+    a = FlatUnit(numels, n_ranks)
+    b = FlatUnit(numels, n_ranks)
+    m0 = synthetic.make_master_flat(a.P, n_ranks, 0.02, ("z1s", n_ranks)).cuda()
+    a.set_master_flat(m0)
+    b.set_master_flat(m0)
+    g = synthetic.make_grads(a.P, n_ranks, 1e-2, ("z1s", n_ranks))
+    gi = g.view(torch.int16)
+    rng = np.random.default_rng(n_ranks)
+    specials = np.array([0x8000, 0x7F80, 0xFF80, 0x7FC0, 0x0001, 0x8001] * 16,
+                        dtype=np.uint16).view(np.int16)
+    for k in sorted({0, n_ranks - 1, n_ranks // 2}):
+        pos = rng.choice(a.P, size=specials.size, replace=False)   # the padding stays zero
+        gi[k, torch.from_numpy(pos)] = torch.from_numpy(specials)
+    gi[:, :64] = torch.tensor(np.uint16(0x8000).view(np.int16))   # every rank -0
+    g = g.cuda()
+    a.grads.copy_(g)
+    b.grads.copy_(g)
+    acc = aligned_rows(n_ranks, a.P_pad, torch.float32, "cuda", 3.0)
+    for t in (1, 2):
+        zf.zero1_accumulate(a.grad_rows(), rows(acc), True, a.layout)
+        zf.zero1_step(rows(acc), 1, *a.state_rows(), a.param_rows(), a.layout, hp_at(t))
+        zf.zero_step(b.grad_rows(), *b.state_rows(), None, 1, 1, b.param_rows(), b.layout,
+                     hp_at(t))
+    torch.cuda.synchronize()
+    for x, y in ((a.master, b.master), (a.m, b.m), (a.v, b.v)):
+        assert torch.equal(x.contiguous().view(torch.int32), y.contiguous().view(torch.int32))
+    assert torch.equal(a.params.contiguous().view(torch.int16),
+                       b.params.contiguous().view(torch.int16))
+    assert zf.zero_device_status() == zf.zero.ZERO_DEVICE_OK
+
